@@ -1,0 +1,434 @@
+"""Benchmark of the MoE dispatch/combine hot path on GB300.
+
+One step = one pass of the whole path over one batch of the DeepSeek-V3-shaped
+workload (8192 tokens, hidden 7168, 256 experts in 8 groups, top-4 groups then
+top-8 experts, 32 logical ranks x 8 experts): group-limited gating -> layout
+-> FP8 e4m3 1x128 dispatch -> weighted BF16 combine of the expert outputs
+(identity experts: the BF16-dispatched rows, made once before timing).
+
+Prints ONE JSON line (rank 0): whole-job tokens/s, per-op times and HBM
+GB/s, the roofline of the dominant kernel, an end-to-end figure through the
+public API with host buffers, the CPU oracle as a baseline, and SM clocks
+sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank runs an independent replica on its own
+batch (weak scaling, no collective on the data path); the time is the max
+over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of peak), 1×GB300"
+WORKLOAD = "dsv3"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20          # twice the 129 MB L2
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def workload_desc(cfg):
+    return ("DeepSeek-V3-shaped MoE layer: T=%d H=%d E=%d in %d groups, top-%d groups then top-%d experts, "
+            "%d logical ranks x %d experts; FP8 e4m3 1x128 dispatch, BF16 combine"
+            % (cfg["T"], cfg["H"], cfg["E"], cfg["n_groups"], cfg["topk_group"], cfg["k"],
+               cfg["E"] // cfg["experts_per_rank"], cfg["experts_per_rank"]))
+
+
+def algorithmic_bytes(cfg):
+    """Bytes each op must move at least (per launch over the whole batch)."""
+    T, H, E, k = cfg["T"], cfg["H"], cfg["E"], cfg["k"]
+    return {
+        "gate": T * (4 * E + 8 * k) + (4 * E if cfg["bias"] else 0),
+        "layout": T * k * 4 * 3,                                        # idx in, pos + src out
+        "dispatch_fp8": T * (2 * H + k * (H + 4 * (H // 128)) + 4 * k),
+        "dispatch_bf16": T * (2 * H + 2 * H * k + 4 * k),
+        "combine": T * (2 * H * k + 8 * k + 2 * H),
+    }
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_group_limited_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernels as they are now (same source hash); else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    v = d.get("per_launch_bytes", {}).get(op)
+    return None if v is None else int(v)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks / throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+class PathRunner:
+    """Device buffers and launches of one step of the hot path (rank-local)."""
+
+    def __init__(self, cfg, seed_offset=0, device="cuda"):
+        import torch
+
+        import combine_group_limited_gb300 as ep
+        self.torch, self.ep, self.cfg = torch, ep, dict(cfg)
+        self.cfg["seed"] = cfg["seed"] + seed_offset
+        c = self.cfg
+        T, H, E, k, epr = c["T"], c["H"], c["E"], c["k"], c["experts_per_rank"]
+        inp = synth.make_inputs(c)
+        self.host = inp
+        self.scores = torch.from_numpy(inp["scores"]).to(device)
+        self.bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(device)
+        self.x = torch.from_numpy(inp["x"].view(np.int16)).to(device).view(torch.bfloat16)
+        self.gcfg = ep.gate_cfg(E, k, c["n_groups"], c["topk_group"], c["topk_in_group"], c["score_fn"],
+                                c["normalize"])
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.lay = ep.alloc_layout(T, k, E, epr, device)
+        self.ws = ep.alloc_layout_workspace(T, k, E, epr, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.recv_q = torch.empty((T * k, H), dtype=torch.uint8, device=device)
+        self.recv_s = torch.empty((T * k, H // 128), dtype=torch.float32, device=device)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        # expert outputs for the combine: identity experts = the BF16 rows
+        self.gate()
+        self.layout()
+        self.y = ep.ep_dispatch(self.x, self.lay.pos, "bf16")
+        torch.cuda.synchronize()
+
+    # the four launches of a step (gpu_launches counts them: 1 + 3 + 1 + 1)
+    LAUNCHES_PER_STEP = 6
+
+    def gate(self):
+        self.ep.ep_gate(self.scores, self.bias, self.gcfg, self.topk_idx, self.topk_w)
+
+    def layout(self):
+        c = self.cfg
+        self.ep.ep_get_layout(self.topk_idx, c["E"], c["experts_per_rank"], out=self.lay, workspace=self.ws,
+                              err_flag=self.err)
+
+    def dispatch(self):
+        self.ep.ep_dispatch(self.x, self.lay.pos, "fp8", recv=self.recv_q, recv_scales=self.recv_s,
+                            err_flag=self.err)
+
+    def combine(self):
+        self.ep.ep_combine(self.y, self.lay.pos, self.topk_w, out=self.out, err_flag=self.err)
+
+    def step(self):
+        self.gate()
+        self.layout()
+        self.dispatch()
+        self.combine()
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from combine_group_limited_gb300 import build as epbuild
+    epbuild.build()
+
+    cfg = synth.config(WORKLOAD)
+    r = PathRunner(cfg, seed_offset=1000 * rank)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ops = ("gate", "layout", "dispatch", "combine")
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        r.step()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)                       # evict L2 between steps (outside the events)
+            ev[s][0].record(stream)
+            for i, op in enumerate(ops):
+                getattr(r, op)()
+                ev[s][i + 1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if int(r.err.item()) != 0:
+        raise RuntimeError("device error flag set: %d" % int(r.err.item()))
+
+    per_op = {op: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)] for i, op in enumerate(ops)}
+    step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
+    ms_per_step = sum(step_ms) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    # end to end through the public API: pinned host inputs -> device -> path -> host output
+    e2e = run_e2e(r, args)
+    if world > 1:
+        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms"] = float(t.item())
+
+    if rank == 0:
+        T = cfg["T"]
+        peak, peak_kind = measured_hbm_peak()
+        ab = algorithmic_bytes(cfg)
+        bytes_of = {"gate": ab["gate"], "layout": ab["layout"], "dispatch": ab["dispatch_fp8"],
+                    "combine": ab["combine"]}
+        kname = {"gate": "gate_kernel", "layout": "layout_*_kernel", "dispatch": "dispatch_fp8_kernel",
+                 "combine": "combine_kernel"}
+        op_summary = {}
+        for op in ops:
+            us = 1e3 * statistics.mean(per_op[op])
+            gbs = bytes_of[op] / (us * 1e-6) / 1e9
+            op_summary[op] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "bytes": bytes_of[op], "kernel": kname[op]}
+        dom = max(("dispatch", "combine"), key=lambda o: op_summary[o]["us"])
+        traffic = recorded_traffic(kname[dom])
+        cpu = cpu_baseline(cfg, args) if world == 1 or rank == 0 else None
+        line = {
+            "metric": METRIC,
+            "value": round(world * T / (ms_per_step * 1e-3), 1),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "fp32",
+            "data": "synthetic (seeded splitmix64: U(0,1) scores, N(0,0.01) bias, N(0,1) bf16 hidden rows)",
+            "config": {"workload": workload_desc(cfg), "T": T, "H": cfg["H"], "E": cfg["E"], "k": cfg["k"],
+                       "n_groups": cfg["n_groups"], "topk_group": cfg["topk_group"],
+                       "logical_ranks": cfg["E"] // cfg["experts_per_rank"],
+                       "payload": "bf16 rows in, e4m3+fp32 1x128 scales dispatched, bf16 expert outputs combined",
+                       "l2": "flushed between steps (256 MB write outside the timed events)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "ops": op_summary,
+            "roofline": {"bound": "hbm", "kernel": kname[dom], "achieved": op_summary[dom]["GB/s"],
+                         "peak": peak, "peak_source": "%s (MEASURED_PEAKS.json hbm)" % peak_kind
+                         if peak_kind == "measured" else "fallback 6.8 TB/s", "unit": "GB/s",
+                         "frac": op_summary[dom]["frac"], "traffic": traffic,
+                         "algorithmic_bytes": bytes_of[dom]},
+            "e2e": {"value": round(world * T / (e2e["ms"] * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "ms_per_step": round(e2e["ms"], 4)},
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+            "gpu_launches": PathRunner.LAUNCHES_PER_STEP * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(r, args):
+    """Same path through the public API, with the step's inputs copied in from
+    pinned host memory and its output copied back, inside the timed region."""
+    import torch
+    hs = torch.from_numpy(r.host["scores"]).pin_memory()
+    hb = None if r.host["bias"] is None else torch.from_numpy(r.host["bias"]).pin_memory()
+    hx = torch.from_numpy(r.host["x"].view(np.int16)).pin_memory()
+    ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
+    stream = torch.cuda.current_stream()
+    n = max(1, min(args.steps, 10))
+
+    def one():
+        r.scores.copy_(hs, non_blocking=True)
+        if hb is not None:
+            r.bias.copy_(hb, non_blocking=True)
+        r.x.view(torch.int16).copy_(hx, non_blocking=True)
+        r.step()
+        ho.copy_(r.out.view(torch.int16), non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        one()
+    b.record(stream)
+    b.synchronize()
+    h2d = hs.numel() * 4 + (0 if hb is None else hb.numel() * 4) + hx.numel() * 2
+    return {"ms": a.elapsed_time(b) / n, "h2d": h2d, "d2h": ho.numel() * 2}
+
+
+def _oracle_path(cfg, inp, y_bits):
+    import oracle
+    idx, w = oracle.gate(inp["scores"], inp["bias"], cfg["k"], cfg["n_groups"], cfg["topk_group"],
+                         cfg["topk_in_group"], cfg["score_fn"], cfg["normalize"])
+    lay = oracle.layout(idx, cfg["E"], cfg["experts_per_rank"])
+    oracle.dispatch_fp8(inp["x"], lay["pos"])
+    oracle.combine(y_bits, lay["pos"], w.astype(np.float32))
+
+
+def _oracle_inputs(cfg):
+    import oracle
+    inp = synth.make_inputs(cfg)
+    idx, _ = oracle.gate(inp["scores"], inp["bias"], cfg["k"], cfg["n_groups"], cfg["topk_group"],
+                         cfg["topk_in_group"], cfg["score_fn"], cfg["normalize"])
+    lay = oracle.layout(idx, cfg["E"], cfg["experts_per_rank"])
+    y = oracle.dispatch_bf16(inp["x"], lay["pos"])     # identity experts, made outside the timing
+    return inp, y
+
+
+def cpu_baseline(cfg, args, tokens=None, reps=3):
+    """The CPU oracle (single-threaded C, as it stands) on the same workload."""
+    tokens = tokens or cfg["T"]
+    c = synth.config(WORKLOAD, T=tokens)
+    inp, y = _oracle_inputs(c)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _oracle_path(c, inp, y)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": round(tokens / t, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "host_cores": os.cpu_count(),
+            "sample": "%d tokens of the same workload through gate+layout+FP8 dispatch+combine, median of %d runs"
+                      % (tokens, reps)}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, as it stands, on this workload."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    cfg = synth.config(WORKLOAD)
+    per_token_s = 0.45e-3
+    n_steps = args.steps + args.warmup
+    tokens = int(120.0 / max(n_steps, 1) / per_token_s) // 64 * 64
+    tokens = max(64, min(cfg["T"], tokens))
+    c = synth.config(WORKLOAD, T=tokens)
+    inp, y = _oracle_inputs(c)
+    for _ in range(args.warmup):
+        _oracle_path(c, inp, y)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_path(c, inp, y)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = round(tokens / (ms * 1e-3), 1)
+    sample = "%d of the workload's %d tokens per step through gate+layout+FP8 dispatch+combine" % (tokens, cfg["T"])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "T": cfg["T"], "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": 1,
+                         "host_cores": os.cpu_count(), "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

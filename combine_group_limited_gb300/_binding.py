@@ -1,0 +1,216 @@
+"""ctypes binding of ``libep_gb300.so`` (the C ABI of ``include/ep.h``).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  Outputs may be
+passed in (pre-allocated, as the pages' operators expect) or are allocated
+here with ``torch.empty``.  There is no fallback: if the library is not built
+the import of this module's functions fails with an error that says so.
+"""
+import ctypes
+import os
+from collections import namedtuple
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libep_gb300.so")
+
+EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_ALIGNMENT, EP_ERR_CUDA = range(5)
+EP_FLAG_BAD_EXPERT, EP_FLAG_BAD_ROW = 1, 2
+EP_SCORE_RAW, EP_SCORE_SOFTMAX = 0, 1
+EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128 = 0, 1
+
+# Symbols include/ep.h declares (checked by the CPU test suite).
+EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_dispatch", "ep_combine",
+           "ep_status_str")
+
+
+class GateCfg(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32), ("n_groups", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("topk_in_group", ctypes.c_int32), ("score_fn", ctypes.c_int32),
+                ("normalize", ctypes.c_int32)]
+
+
+class EpError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, status_str(status), status))
+
+
+_lib = None
+
+
+def load():
+    """Load libep_gb300.so (built by ``combine_group_limited_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libep_gb300.so is not built (expected at %s); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.ep_gate.argtypes = [P, P, i32, ctypes.POINTER(GateCfg), P, P, P]
+    lib.ep_layout_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.ep_layout_workspace_bytes.restype = sz
+    lib.ep_get_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.ep_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, P, P, P]
+    lib.ep_combine.argtypes = [P, P, P, i32, i32, i32, P, P, P]
+    for f in ("ep_gate", "ep_get_layout", "ep_dispatch", "ep_combine"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.ep_status_str.argtypes = [ctypes.c_int]
+    lib.ep_status_str.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_str(status):
+    return load().ep_status_str(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != EP_OK:
+        raise EpError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+
+
+def _dev(t, dtype, name, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def gate_cfg(num_experts, top_k, n_groups=1, topk_group=1, topk_in_group=1, score_fn=EP_SCORE_RAW, normalize=True):
+    return GateCfg(num_experts, top_k, n_groups, topk_group, topk_in_group, score_fn, int(bool(normalize)))
+
+
+def ep_gate(scores, bias, cfg, topk_idx=None, topk_w=None, stream=None):
+    """Step 1.  scores fp32 [T,E], bias fp32 [E] or None -> (topk_idx int32 [T,k], topk_w fp32 [T,k])."""
+    lib = load()
+    _dev(scores, torch.float32, "scores")
+    T = scores.shape[0]
+    k = cfg.top_k
+    if bias is not None:
+        _dev(bias, torch.float32, "bias", (cfg.num_experts,))
+    if scores.dim() != 2 or scores.shape[1] != cfg.num_experts:
+        raise ValueError("scores must be [T, num_experts]")
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=scores.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=scores.device)
+    _dev(topk_idx, torch.int32, "topk_idx", (T, k))
+    _dev(topk_w, torch.float32, "topk_w", (T, k))
+    _check("ep_gate", lib.ep_gate(_ptr(scores), _ptr(bias), T, ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w),
+                                  _stream(stream)))
+    return topk_idx, topk_w
+
+
+Layout = namedtuple("Layout", "expert_count expert_off rank_count rank_off rank_tokens pos src")
+
+
+def ep_layout_workspace_bytes(T, k, E, experts_per_rank):
+    return int(load().ep_layout_workspace_bytes(T, k, E, experts_per_rank))
+
+
+def alloc_layout(T, k, E, experts_per_rank, device="cuda"):
+    R = E // experts_per_rank
+    z = lambda *s: torch.empty(s, dtype=torch.int32, device=device)  # noqa: E731
+    return Layout(z(E), z(E + 1), z(R), z(R + 1), z(R), z(T, k), z(T * k))
+
+
+def alloc_layout_workspace(T, k, E, experts_per_rank, device="cuda"):
+    n = ep_layout_workspace_bytes(T, k, E, experts_per_rank)
+    if n == 0:
+        raise ValueError("invalid layout sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def ep_get_layout(topk_idx, num_experts, experts_per_rank, out=None, workspace=None, err_flag=None, stream=None):
+    """Step 2.  topk_idx int32 [T,k] -> Layout of int32 device tensors."""
+    lib = load()
+    _dev(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    E, epr = num_experts, experts_per_rank
+    if out is None:
+        out = alloc_layout(T, k, E, epr, topk_idx.device) if epr > 0 and E % epr == 0 else None
+    if out is None:
+        raise ValueError("experts_per_rank must divide num_experts")
+    if workspace is None:
+        workspace = alloc_layout_workspace(T, k, E, epr, topk_idx.device)
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_get_layout", lib.ep_get_layout(
+        _ptr(topk_idx), T, k, E, epr, _ptr(out.expert_count), _ptr(out.expert_off), _ptr(out.rank_count),
+        _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.pos), _ptr(out.src), _ptr(err_flag),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def ep_dispatch(x, pos, dtype="bf16", recv=None, recv_scales=None, err_flag=None, stream=None):
+    """Step 3.  x bf16 [T,H], pos int32 [T,k].
+
+    dtype "bf16" -> recv bf16 [T*k, H];
+    dtype "fp8"  -> (recv uint8 e4m3 codes [T*k, H], recv_scales fp32 [T*k, H/128]).
+    """
+    lib = load()
+    _dev(x, torch.bfloat16, "x")
+    _dev(pos, torch.int32, "pos")
+    T, H = x.shape
+    k = pos.shape[1]
+    if pos.shape[0] != T:
+        raise ValueError("pos must be [T, k]")
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    if dtype == "bf16":
+        if recv is None:
+            recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+        _dev(recv, torch.bfloat16, "recv", (T * k, H))
+        _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos), EP_DTYPE_BF16, _ptr(recv), None,
+                                              _ptr(err_flag), _stream(stream)))
+        return recv
+    if dtype != "fp8":
+        raise ValueError("dtype must be 'bf16' or 'fp8'")
+    if recv is None:
+        recv = torch.empty((T * k, H), dtype=torch.uint8, device=x.device)
+    if recv_scales is None:
+        recv_scales = torch.empty((T * k, max(H // 128, 1)), dtype=torch.float32, device=x.device)
+    _dev(recv, torch.uint8, "recv", (T * k, H))
+    _dev(recv_scales, torch.float32, "recv_scales")
+    _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos), EP_DTYPE_FP8_E4M3_B128, _ptr(recv),
+                                          _ptr(recv_scales), _ptr(err_flag), _stream(stream)))
+    return recv, recv_scales
+
+
+def ep_combine(y, pos, topk_w, out=None, err_flag=None, stream=None):
+    """Steps 4-5.  y bf16 [T*k, H], pos int32 [T,k], topk_w fp32 [T,k] -> out bf16 [T,H]."""
+    lib = load()
+    _dev(y, torch.bfloat16, "y")
+    _dev(pos, torch.int32, "pos")
+    T, k = pos.shape
+    _dev(topk_w, torch.float32, "topk_w", (T, k))
+    H = y.shape[1]
+    if y.shape[0] != T * k:
+        raise ValueError("y must have T*k rows")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _dev(out, torch.bfloat16, "out", (T, H))
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_combine", lib.ep_combine(_ptr(y), _ptr(pos), _ptr(topk_w), T, H, k, _ptr(out), _ptr(err_flag),
+                                        _stream(stream)))
+    return out

@@ -1,0 +1,177 @@
+// ep_api.cu -- the C ABI declared in include/ep.h: argument checks, then the
+// launches.  No allocation, no host synchronisation.
+#include <stdint.h>
+
+#include "ep.h"
+#include "ep_internal.cuh"
+
+namespace ep {
+
+int device_sm_count()
+{
+    // Cached per device; the attribute never changes for a device.
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 1;
+    if (dev < 64 && cache[dev] > 0)
+        return cache[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
+}  // namespace ep
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+ep_status launched(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+constexpr int kMaxGateExperts = 512;
+constexpr int kMaxGateK = 32;
+constexpr int kMaxGroups = 32;
+constexpr int kMaxKin = 4;
+constexpr int kMaxLayoutExperts = 1024;
+constexpr int kMaxRowK = 64;
+
+ep_status check_layout_args(int32_t T, int32_t k, int32_t E, int32_t epr)
+{
+    if (T < 0 || k < 1 || E < 1 || epr < 1 || E % epr != 0)
+        return EP_ERR_INVALID_ARG;
+    if (E > kMaxLayoutExperts || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ep_status_str(ep_status s)
+{
+    switch (s) {
+    case EP_OK:
+        return "ok";
+    case EP_ERR_INVALID_ARG:
+        return "invalid argument";
+    case EP_ERR_UNSUPPORTED:
+        return "unsupported size or configuration";
+    case EP_ERR_ALIGNMENT:
+        return "misaligned pointer";
+    case EP_ERR_CUDA:
+        return "CUDA launch error";
+    }
+    return "unknown status";
+}
+
+ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg, int32_t *topk_idx,
+                  float *topk_w, void *stream)
+{
+    if (!cfg || T < 0)
+        return EP_ERR_INVALID_ARG;
+    const int E = cfg->num_experts, k = cfg->top_k, G = cfg->n_groups, Kg = cfg->topk_group;
+    const int kin = cfg->topk_in_group;
+    if (E < 1 || k < 1 || k > E || G < 1 || E % G != 0 || Kg < 1 || Kg > G || kin < 1 || kin > E / G)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)Kg * (E / G) < k)
+        return EP_ERR_INVALID_ARG;
+    if (cfg->score_fn != EP_SCORE_RAW && cfg->score_fn != EP_SCORE_SOFTMAX)
+        return EP_ERR_INVALID_ARG;
+    if (cfg->normalize != 0 && cfg->normalize != 1)
+        return EP_ERR_INVALID_ARG;
+    if (E > kMaxGateExperts || k > kMaxGateK || G > kMaxGroups || kin > kMaxKin)
+        return EP_ERR_UNSUPPORTED;
+    if ((int64_t)T * E >= (int64_t)1 << 40)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if (!scores || !topk_idx || !topk_w)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || (bias && !aligned(bias, 4)) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+        return EP_ERR_ALIGNMENT;
+    ep::GateParams p{E, k, G, Kg, kin, cfg->score_fn, cfg->normalize};
+    return launched(ep::launch_gate(scores, bias, T, p, topk_idx, topk_w, static_cast<cudaStream_t>(stream)));
+}
+
+size_t ep_layout_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t experts_per_rank)
+{
+    if (check_layout_args(T, k, E, experts_per_rank) != EP_OK)
+        return 0;
+    return ep::layout_workspace_bytes(T, k, E, experts_per_rank);
+}
+
+ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E, int32_t experts_per_rank,
+                        int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                        int32_t *rank_tokens, int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    const ep_status a = check_layout_args(T, k, E, experts_per_rank);
+    if (a != EP_OK)
+        return a;
+    if (!expert_count || !expert_off || !rank_count || !rank_off || !rank_tokens || !workspace)
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !pos || !src))
+        return EP_ERR_INVALID_ARG;
+    if (workspace_bytes < ep::layout_workspace_bytes(T, k, E, experts_per_rank))
+        return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {topk_idx, expert_count, expert_off, rank_count, rank_off, rank_tokens, pos, src, err_flag};
+    for (const void *q : ptrs)
+        if (q && !aligned(q, 4))
+            return EP_ERR_ALIGNMENT;
+    if (!aligned(workspace, 16))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_layout(topk_idx, T, k, E, experts_per_rank, expert_count, expert_off, rank_count,
+                                      rank_off, rank_tokens, pos, src, err_flag, workspace,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_dispatch(const void *x, int32_t T, int32_t H, int32_t k, const int32_t *pos, int32_t dtype, void *recv,
+                      float *recv_scales, int32_t *err_flag, void *stream)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return EP_ERR_INVALID_ARG;
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128)
+        return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (dtype == EP_DTYPE_FP8_E4M3_B128 && H % 128 != 0)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if (!x || !pos || !recv || (dtype == EP_DTYPE_FP8_E4M3_B128 && !recv_scales))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(pos, 4) || (recv_scales && !aligned(recv_scales, 4)) ||
+        (err_flag && !aligned(err_flag, 4)))
+        return EP_ERR_ALIGNMENT;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == EP_DTYPE_BF16)
+        return launched(ep::launch_dispatch_bf16(static_cast<const uint16_t *>(x), T, H, k, pos,
+                                                 static_cast<uint16_t *>(recv), err_flag, st));
+    return launched(ep::launch_dispatch_fp8(static_cast<const uint16_t *>(x), T, H, k, pos,
+                                            static_cast<uint8_t *>(recv), recv_scales, err_flag, st));
+}
+
+ep_status ep_combine(const void *y, const int32_t *pos, const float *topk_w, int32_t T, int32_t H, int32_t k,
+                     void *out, int32_t *err_flag, void *stream)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if (!y || !pos || !topk_w || !out)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(pos, 4) || !aligned(topk_w, 4) ||
+        (err_flag && !aligned(err_flag, 4)))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_combine(static_cast<const uint16_t *>(y), pos, topk_w, T, H, k,
+                                       static_cast<uint16_t *>(out), err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

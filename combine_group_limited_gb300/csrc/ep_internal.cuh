@@ -1,0 +1,89 @@
+// ep_internal.cuh -- shared device helpers and kernel launchers of the
+// MoE dispatch/combine library (sm_103a).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ep {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+// Order-preserving map of a binary32 value onto uint32: a < b as floats
+// iff key(a) < key(b) as integers.  -0.0 maps like +0.0 so that equal floats
+// give equal keys (ties are then broken by index).  NaN inputs are
+// unsupported.
+__device__ __forceinline__ uint32_t ordered_key(float v)
+{
+    uint32_t u = __float_as_uint(v);
+    if (u == 0x80000000u)
+        u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two bf16 (round to nearest even) packed lo | hi << 16.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two fp32 values -> two e4m3 codes (round to nearest even, saturating to
+// the largest finite magnitude) packed lo | hi << 8.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// 16-byte global load that bypasses L1 allocation (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte global store with the streaming (evict-first) cache hint.
+__device__ __forceinline__ void st_stream16(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+struct GateParams {
+    int E, k, G, Kg, kin, score_fn, normalize;
+};
+
+// Launchers (return the launch's cudaGetLastError()).
+cudaError_t launch_gate(const float *scores, const float *bias, int T, const GateParams &p,
+                        int32_t *topk_idx, float *topk_w, cudaStream_t st);
+
+int layout_tile_tokens(int k);
+int layout_num_tiles(int T, int k);
+size_t layout_workspace_bytes(int T, int k, int E, int epr);
+cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr, int32_t *expert_count,
+                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                          int32_t *rank_tokens, int32_t *pos, int32_t *src, int32_t *err_flag,
+                          void *workspace, cudaStream_t st);
+
+cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const int32_t *pos,
+                                 uint16_t *recv, int32_t *err_flag, cudaStream_t st);
+cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const int32_t *pos,
+                                uint8_t *recv_q, float *recv_s, int32_t *err_flag, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t *y, const int32_t *pos, const float *w, int T, int H, int k,
+                           uint16_t *out, int32_t *err_flag, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace ep

@@ -1,0 +1,198 @@
+/*
+ * ep.h -- C ABI of the MoE expert-parallel dispatch/combine hot path on one
+ * GB300 (sm_103a): group-limited top-k gating, dispatch layout,
+ * permute-scatter (BF16, or FP8 e4m3 with 1x128 block scales), inverse gather
+ * and router-weighted combine.
+ *
+ * The operation follows the pages' statement of expert parallelism:
+ *  - "Expert Parallelism (Parallelisme d'experts)" (polydesk.ai glossary),
+ *    section "Le principe de base": whole experts live on a rank, E experts
+ *    over E/experts_per_rank ranks; section "Le pattern de communication
+ *    all-to-all": Phase 1 Dispatch sends each token to the holders of its
+ *    chosen experts, Phase 2 Combine returns the expert outputs and sums them
+ *    weighted by the router scores.
+ *  - "DeepEP de DeepSeek : la lib open source qui optimise la communication
+ *    GPU pour les modeles MoE a l'echelle" (ai-master.dev), section
+ *    "Group-limited gating algorithm" (experts chosen inside a few groups),
+ *    section "Support FP8 et MXFP8" (FP8 payload at half the BF16 bytes).
+ *  - hyper.ai story on NVIDIA Hybrid-EP (hyper.ai/fr/stories/b564891f...):
+ *    dispatch/combine operators callable from PyTorch over pre-allocated
+ *    buffers; sizing them must not need a host round trip when a fixed
+ *    maximum is known.
+ *
+ * On one GPU the "ranks" are logical: rank r owns experts
+ * [r*experts_per_rank, (r+1)*experts_per_rank) and the rows of one receive
+ * buffer between rank_off[r] and rank_off[r+1].  A send is a store.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates or frees device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
+ *    NULL = legacy default stream) and never synchronise the host.
+ *  - Problems that the host can see (bad sizes, bad configuration, NULL or
+ *    misaligned pointers) return an error status and launch nothing.
+ *    A failed launch returns EP_ERR_CUDA (the CUDA error is left to
+ *    cudaGetLastError's caller to inspect or clear).
+ *  - Problems only the device can see never trap: the offending entry is
+ *    skipped and a bit is OR-ed into *err_flag (a device int32, may be NULL):
+ *      EP_FLAG_BAD_EXPERT  an expert index neither -1 nor in [0, E)
+ *      EP_FLAG_BAD_ROW     a receive row outside [0, T*k)
+ *  - bf16 tensors are raw 16-bit bfloat16 patterns, row-major.
+ *  - T*k rows always suffice for a receive buffer (top-k picks k distinct
+ *    experts per token), so buffers are sized without reading any count
+ *    back to the host.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1, /* a size, pointer or configuration field is invalid */
+    EP_ERR_UNSUPPORTED = 2, /* valid in principle but outside this library's limits */
+    EP_ERR_ALIGNMENT = 3,   /* a pointer is not aligned as the call requires */
+    EP_ERR_CUDA = 4         /* the CUDA runtime reported an error at launch */
+} ep_status;
+
+enum { EP_FLAG_BAD_EXPERT = 1, EP_FLAG_BAD_ROW = 2 };
+
+typedef enum {
+    EP_SCORE_RAW = 0,    /* scores are affinities used as given (e.g. sigmoid outputs) */
+    EP_SCORE_SOFTMAX = 1 /* scores are logits; weights come from their softmax */
+} ep_score_fn;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,         /* receive rows are bf16 copies of x */
+    EP_DTYPE_FP8_E4M3_B128 = 1 /* receive rows are e4m3 codes + one fp32 scale per 128 columns */
+} ep_dtype;
+
+/* Gating configuration (see ep_gate). */
+typedef struct {
+    int32_t num_experts;   /* E, 1..512 */
+    int32_t top_k;         /* k, 1..min(E, 32) */
+    int32_t n_groups;      /* G, 1..32, divides E; groups are contiguous blocks of E/G experts */
+    int32_t topk_group;    /* groups kept per token, 1..G; topk_group * E/G >= k */
+    int32_t topk_in_group; /* keys summed into a group's score, 1..min(4, E/G) */
+    int32_t score_fn;      /* ep_score_fn */
+    int32_t normalize;     /* 1: weights of a token sum to one; 0: unnormalised */
+} ep_gate_cfg;
+
+/*
+ * Step 1 -- router top-k with the group limit ("DeepEP de DeepSeek ...",
+ * section "Group-limited gating algorithm"; hyper.ai Hybrid-EP story: each
+ * token activates only its top-k experts).
+ *
+ * scores   [T, E] fp32 row-major: affinities (RAW) or logits (SOFTMAX).
+ * bias     [E] fp32 or NULL: added to the score to form the selection key
+ *          (key = score + bias, fp32); it never enters the weights.
+ * T        tokens, >= 0.
+ * topk_idx [T, k] int32 out: chosen experts in slot order = selection order
+ *          (descending key; equal keys -> lower expert index first).
+ * topk_w   [T, k] fp32 out: RAW: score (normalize=0) or score / sum of the
+ *          chosen scores in slot order (normalize=1). SOFTMAX: the full
+ *          softmax probability (normalize=0) or exp(l - m) / sum over the
+ *          chosen k of exp(l - m), m = largest chosen logit (normalize=1).
+ * Group score = sum of the group's topk_in_group largest keys, largest
+ * first, in fp32; the topk_group best groups are kept (ties -> lower group
+ * index) and the k experts are chosen among them.  With n_groups = 1 this is
+ * plain top-k.  Scores must be finite.
+ * Errors: EP_ERR_INVALID_ARG (NULL pointer with T > 0, cfg fields out of
+ * range), EP_ERR_UNSUPPORTED (E > 512, k > 32, G > 32, topk_in_group > 4),
+ * EP_ERR_ALIGNMENT (scores, bias, outputs not 4-byte aligned), EP_ERR_CUDA.
+ */
+ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
+                  int32_t *topk_idx, float *topk_w, void *stream);
+
+/* Bytes of device workspace ep_get_layout needs for these sizes (a multiple
+ * of 256; 0 if the sizes are invalid). */
+size_t ep_layout_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t experts_per_rank);
+
+/*
+ * Step 2 -- dispatch layout for logical ranks of experts_per_rank contiguous
+ * experts ("Expert Parallelism ...", section "Le principe de base"; the
+ * hyper.ai Hybrid-EP story's buffer sizing step).
+ *
+ * topk_idx      [T, k] int32: expert per (token, slot); -1 = empty slot.
+ * expert_count  [E] out: entries per expert.
+ * expert_off    [E+1] out: exclusive prefix sum of expert_count.
+ * rank_count    [R] out (R = E / experts_per_rank): entries per rank.
+ * rank_off      [R+1] out: exclusive prefix sum of rank_count.
+ * rank_tokens   [R] out: distinct tokens with at least one entry on the rank.
+ * pos           [T, k] out: receive row of entry (t, j) = expert_off[e] +
+ *               number of entries of expert e with a smaller flat index
+ *               t*k+j (a stable order), or -1 for a skipped entry.
+ * src           [T*k] out: inverse of pos (flat entry index per receive
+ *               row); rows at or past expert_off[E] hold -1.
+ * err_flag      device int32 or NULL: EP_FLAG_BAD_EXPERT is OR-ed in when an
+ *               index is neither -1 nor in [0, E); that entry is skipped.
+ * workspace     device scratch of at least ep_layout_workspace_bytes(...)
+ *               bytes, 16-byte aligned; contents need no initialisation and
+ *               are garbage afterwards.  It must not be shared by layouts
+ *               in flight at the same time.
+ * Limits: 1 <= E <= 1024, experts_per_rank divides E, k >= 1, T >= 0,
+ * T*k < 2^31.  Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED,
+ * EP_ERR_ALIGNMENT, EP_ERR_CUDA.
+ */
+ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E,
+                        int32_t experts_per_rank, int32_t *expert_count, int32_t *expert_off,
+                        int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                        int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
+ * Step 3 -- permute-scatter ("Expert Parallelism ...", section "Le pattern
+ * de communication all-to-all", Phase 1; FP8 mode from "DeepEP de DeepSeek
+ * ...", section "Support FP8 et MXFP8").
+ *
+ * x            [T, H] bf16, 16-byte aligned; H % 8 == 0.
+ * pos          [T, k] int32 receive row per entry (from ep_get_layout);
+ *              entries < 0 are skipped; rows >= T*k are skipped and flagged
+ *              EP_FLAG_BAD_ROW.
+ * dtype        EP_DTYPE_BF16: recv [T*k, H] bf16, recv[pos[t,j]] = x[t].
+ *              EP_DTYPE_FP8_E4M3_B128 (needs H % 128 == 0): recv [T*k, H]
+ *              e4m3 bytes and recv_scales [T*k, H/128] fp32; per token and
+ *              128-column block b: s = amax|x[t, b]| / 448 (fp32 IEEE
+ *              division), code = e4m3(x / s) with an fp32 IEEE division and
+ *              round-to-nearest-even saturating to +-448; a block with
+ *              amax = 0 gets s = 0 and signed-zero codes.  Every copy of a
+ *              token carries the same codes and scales.
+ * recv         16-byte aligned.  recv_scales: 4-byte aligned, NULL for BF16.
+ * Rows of recv not named by pos are left untouched.
+ * Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED (FP8 with H % 128 != 0),
+ * EP_ERR_ALIGNMENT, EP_ERR_CUDA.
+ */
+ep_status ep_dispatch(const void *x, int32_t T, int32_t H, int32_t k, const int32_t *pos,
+                      int32_t dtype, void *recv, float *recv_scales, int32_t *err_flag,
+                      void *stream);
+
+/*
+ * Steps 4 and 5 -- inverse gather and weighted combine ("Expert Parallelism
+ * ...", section "Le pattern de communication all-to-all", Phase 2: results
+ * return to their token and are combined weighted by the router scores).
+ *
+ * y       [T*k, H] bf16 expert outputs in receive-row order, 16-byte aligned.
+ * pos     [T, k] int32 (from ep_get_layout); entries < 0 contribute nothing,
+ *         rows >= T*k contribute nothing and are flagged EP_FLAG_BAD_ROW.
+ * topk_w  [T, k] fp32 router weights.
+ * out     [T, H] bf16, 16-byte aligned:
+ *         out[t, h] = bf16_rne( fma chain over j = 0..k-1 in slot order of
+ *         w[t, j] * y[pos[t, j], h], accumulated in fp32 from 0 ).
+ * H % 8 == 0.  Errors: EP_ERR_INVALID_ARG, EP_ERR_ALIGNMENT, EP_ERR_CUDA.
+ */
+ep_status ep_combine(const void *y, const int32_t *pos, const float *topk_w, int32_t T, int32_t H,
+                     int32_t k, void *out, int32_t *err_flag, void *stream);
+
+/* Static description of a status code. */
+const char *ep_status_str(ep_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

@@ -1,0 +1,37 @@
+"""The benchmark's own step, in the launch configuration bench.py times, at
+the full DeepSeek-V3-shaped size, checked end to end against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import assert_combine_close, assert_weights_close, gate_args, host_bits, weight_rtol
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bench_step_matches_oracle():
+    import bench
+    cfg = synth.config(bench.WORKLOAD)
+    r = bench.PathRunner(cfg)
+    for _ in range(2):                       # a repeated step must give the same answer
+        r.step()
+    torch.cuda.synchronize()
+    assert int(r.err.item()) == 0
+    inp = r.host
+    oi, ow = oracle.gate(inp["scores"], inp["bias"], *gate_args(cfg))
+    np.testing.assert_array_equal(r.topk_idx.cpu().numpy(), oi)
+    w = r.topk_w.cpu().numpy()
+    assert_weights_close(w, ow, weight_rtol(cfg, inp["scores"], oi))
+    ol = oracle.layout(oi, cfg["E"], cfg["experts_per_rank"])
+    for key in ("expert_count", "expert_off", "rank_count", "rank_off", "rank_tokens", "src"):
+        np.testing.assert_array_equal(getattr(r.lay, key).cpu().numpy(), ol[key], err_msg=key)
+    pos = r.lay.pos.cpu().numpy()
+    np.testing.assert_array_equal(pos, ol["pos"])
+    oq, os_ = oracle.dispatch_fp8(inp["x"], pos)
+    np.testing.assert_array_equal(r.recv_q.cpu().numpy(), oq)
+    np.testing.assert_array_equal(r.recv_s.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    y = host_bits(r.y)
+    np.testing.assert_array_equal(y, oracle.dispatch_bf16(inp["x"], pos))
+    assert_combine_close(host_bits(r.out), oracle.combine(y, pos, w), y, pos, w)
