@@ -21,8 +21,8 @@ EP_SCORE_RAW, EP_SCORE_SOFTMAX = 0, 1
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128 = 0, 1
 
 # Symbols include/ep.h declares (checked by the CPU test suite).
-EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_dispatch", "ep_combine",
-           "ep_status_str")
+EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch",
+           "ep_combine", "ep_status_str")
 
 
 class GateCfg(ctypes.Structure):
@@ -54,9 +54,10 @@ def load():
     lib.ep_layout_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.ep_layout_workspace_bytes.restype = sz
     lib.ep_get_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.ep_get_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
     lib.ep_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, P, P, P]
     lib.ep_combine.argtypes = [P, P, P, i32, i32, i32, P, P, P]
-    for f in ("ep_gate", "ep_get_layout", "ep_dispatch", "ep_combine"):
+    for f in ("ep_gate", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ep_status_str.argtypes = [ctypes.c_int]
     lib.ep_status_str.restype = ctypes.c_char_p
@@ -158,6 +159,24 @@ def ep_get_layout(topk_idx, num_experts, experts_per_rank, out=None, workspace=N
         _ptr(topk_idx), T, k, E, epr, _ptr(out.expert_count), _ptr(out.expert_off), _ptr(out.rank_count),
         _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.pos), _ptr(out.src), _ptr(err_flag),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def ep_get_layout_noalloc(topk_idx, num_experts, experts_per_rank, out, err_flag=None, stream=None):
+    """Step 2 without a workspace, for callers that cannot allocate device
+    memory at call time (see include/ep.h): the scratch is a fixed array
+    inside the library and ``out`` must be pre-allocated (alloc_layout).
+    Calls that overlap on the GPU share that array and must not run
+    concurrently."""
+    lib = load()
+    _dev(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_get_layout_noalloc", lib.ep_get_layout_noalloc(
+        _ptr(topk_idx), T, k, num_experts, experts_per_rank, _ptr(out.expert_count), _ptr(out.expert_off),
+        _ptr(out.rank_count), _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.pos), _ptr(out.src),
+        _ptr(err_flag), _stream(stream)))
     return out
 
 

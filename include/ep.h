@@ -146,6 +146,32 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
                         size_t workspace_bytes, void *stream);
 
 /*
+ * ep_get_layout without a workspace argument, for callers that cannot
+ * allocate device memory at call time: code running inside another
+ * runtime whose memory pool owns the device memory (a plugin or custom
+ * operator that may not call cudaMalloc itself), or a serving loop with a
+ * memory budget fixed at start-up, where an allocation per call could fail
+ * mid-request or stall the device.  The source pages have no counterpart to
+ * this call; it exists for those callers only.
+ *
+ * Arguments, outputs and errors are those of ep_get_layout.  The scratch is
+ * a fixed 1 MiB device array inside this library (every GPU that loads the
+ * library keeps it until the process exits); sizes whose
+ * ep_layout_workspace_bytes exceeds 1 MiB are rejected with
+ * EP_ERR_UNSUPPORTED (for example T*k up to about 1.8 million entries at
+ * E = 256, experts_per_rank = 8).  The call allocates nothing.  The first
+ * call on a device looks up the array's device address (with that device
+ * current) and caches it: make that first call before any stream capture.
+ * Every call on a device shares the one array, so calls whose work overlaps
+ * on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller; the array needs no clearing between calls.
+ */
+ep_status ep_get_layout_noalloc(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E,
+                                int32_t experts_per_rank, int32_t *expert_count, int32_t *expert_off,
+                                int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                                int32_t *pos, int32_t *src, int32_t *err_flag, void *stream);
+
+/*
  * Step 3 -- permute-scatter ("Expert Parallelism ...", section "Le pattern
  * de communication all-to-all", Phase 1; FP8 mode from "DeepEP de DeepSeek
  * ...", section "Support FP8 et MXFP8").
