@@ -97,51 +97,67 @@ def recorded_traffic(op):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks / throttle reasons during a region."""
+    """nvidia-smi sampling of SM clocks / throttle reasons; only the samples
+    taken between mark_start() and mark_end() (the timed region) count."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index):
-        self.index = index
-        self.proc = None
+    def __init__(self, index, period_ms=20):
+        self.index, self.period_ms = index, period_ms
+        self.proc, self.samples, self.t0, self.t1 = None, [], None, None
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            self.samples.append((time.monotonic(), ln))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.5)
         return self
 
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
+
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
+            time.sleep(2 * self.period_ms / 1000)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self.thread.join(timeout=5)
 
     def summary(self):
         rows = []
-        for ln in getattr(self, "lines", []):
+        for ts, ln in self.samples:
+            if self.t0 is None or not (self.t0 <= ts <= (self.t1 or ts)):
+                continue
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 7:
                 continue
             try:
-                rows.append((float(f[1]), float(f[2]), f[5:9]))
+                rows.append((float(f[0]), float(f[1]), [v.lower() == "active" for v in f[3:7]]))
             except ValueError:
                 continue
         if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample fell inside the timed region"}
+        reasons = sorted({self.NAMES[i] for _, _, r in rows for i, a in enumerate(r) if a})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": reasons, "samples": len(rows)}
 
@@ -233,6 +249,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         for s in range(args.steps):
             flush.fill_(s & 0xFF)                       # evict L2 between steps (outside the events)
             ev[s][0].record(stream)
@@ -240,6 +257,7 @@ def run_ours(args):
                 getattr(r, op)()
                 ev[s][i + 1].record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if world > 1:
         dist.barrier()
     if int(r.err.item()) != 0:
@@ -418,7 +436,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     args = ap.parse_args()

@@ -7,13 +7,17 @@
 // FP8 et MXFP8": an FP8 payload halves the bytes against BF16.
 //
 // HBM-bound: every source row is read once and written k times (BF16: 2H
-// bytes in, 2Hk out; FP8: 2H in, k(H + H/32) out).  A CTA takes one token at
-// a time; its threads cover the row in 16-byte chunks with streaming loads,
-// hold them in registers and issue the k stores (the row is never re-read
-// per copy).  FP8: 8 consecutive lanes own one 128-column block (16 columns
-// each); the block's amax is a 3-step xor-shuffle max, the scale an IEEE
-// fp32 division by 448, each code an IEEE fp32 division then a
-// round-to-nearest-even saturating e4m3 conversion (cvt.rn.satfinite).
+// bytes in, 2Hk out; FP8: 2H in, k(H + H/32) out).  Work is split into warp
+// items -- one token's row segment of 32 lanes x 16 bytes (x U) -- handed out
+// grid-stride to a persistent grid of (resident CTAs per SM) x (SMs).  There
+// is no block barrier: lane j of the warp holds the token's j-th receive row
+// (and lane j of a second register slot j+32) and shuffles it to the others,
+// so every warp streams independently.  Loads bypass L1; stores carry the
+// streaming hint.  The row is held in registers and never re-read per copy.
+// FP8: 8 consecutive lanes own one 128-column block (16 columns each); the
+// block's amax is a 3-step xor-shuffle max, the scale an IEEE fp32 division
+// by 448, each code an IEEE fp32 division then a round-to-nearest-even
+// saturating e4m3 conversion (cvt.rn.satfinite).
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -21,57 +25,100 @@ namespace ep {
 namespace {
 
 constexpr int kDispThreads = 256;
-constexpr int kMaxK = 64;
-constexpr int kBf16Unroll = 4;
+constexpr int kBf16Unroll = 4;   // 16-byte chunks per lane per item (BF16)
 
-// Loads the token's k receive rows into shared memory; bad rows are dropped
-// and flagged.  Ends with a block barrier.
-__device__ __forceinline__ void load_rows(const int32_t *__restrict__ pos, int t, int k, long long rows,
-                                          int32_t *s_pos, int32_t *err_flag)
+// Receive rows of token t for the calling warp: slot `lane` in p0, slot
+// `lane + 32` in p1; -1 where the slot does not exist, is empty, or names a
+// row outside [0, rows) (flagged).
+__device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long long t, int k, long long rows,
+                                           int lane, int32_t *err_flag, int &p0, int &p1)
 {
-    __syncthreads();  // the previous token's readers are done
-    if (threadIdx.x < k) {
-        int p = __ldg(pos + (size_t)t * k + threadIdx.x);
-        if (p >= rows) {
-            if (err_flag)
-                atomicOr(err_flag, 2);
-            p = -1;
-        }
-        s_pos[threadIdx.x] = p;
+    p0 = -1;
+    p1 = -1;
+    if (lane < k)
+        p0 = __ldg(pos + t * k + lane);
+    if (lane + 32 < k)
+        p1 = __ldg(pos + t * k + lane + 32);
+    if (p0 >= rows || p1 >= rows) {
+        if (err_flag)
+            atomicOr(err_flag, 2);
+        if (p0 >= rows)
+            p0 = -1;
+        if (p1 >= rows)
+            p1 = -1;
     }
-    __syncthreads();
 }
+
+__device__ __forceinline__ int slot_row(int p0, int p1, int j)
+{
+    const int a = __shfl_sync(kFullMask, p0, j & 31);
+    const int b = __shfl_sync(kFullMask, p1, j & 31);
+    return j < 32 ? a : b;
+}
+
+// Walks warp items (token, segment) grid-stride without a division per item.
+struct ItemWalk {
+    long long t;
+    int seg;
+    int segs;
+    long long T;
+    int step_seg;
+    long long step_t;
+
+    __device__ ItemWalk(long long T_, int segs_)
+    {
+        T = T_;
+        segs = segs_;
+        const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+        const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+        t = warp / segs;
+        seg = (int)(warp - t * segs);
+        step_t = nwarps / segs;
+        step_seg = (int)(nwarps - step_t * segs);
+    }
+    __device__ bool valid() const { return t < T; }
+    __device__ void next()
+    {
+        t += step_t;
+        seg += step_seg;
+        if (seg >= segs) {
+            seg -= segs;
+            ++t;
+        }
+    }
+};
 
 __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                                      int k, const int32_t *__restrict__ pos,
                                                                      uint16_t *__restrict__ recv,
                                                                      int32_t *__restrict__ err_flag)
 {
-    __shared__ int32_t s_pos[kMaxK];
+    const int lane = threadIdx.x & 31;
     const int C = H / 8;  // 16-byte chunks per row
+    const int segs = (C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll);
     const long long rows = (long long)T * k;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        load_rows(pos, t, k, rows, s_pos, err_flag);
-        const uint16_t *xrow = x + (size_t)t * H;
-        for (int c0 = threadIdx.x; c0 < C; c0 += kDispThreads * kBf16Unroll) {
-            uint4 v[kBf16Unroll];
+    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+        int p0, p1;
+        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
+        const uint16_t *xrow = x + (size_t)it.t * H;
+        const int c0 = it.seg * 32 * kBf16Unroll + lane;
+        uint4 v[kBf16Unroll];
+#pragma unroll
+        for (int u = 0; u < kBf16Unroll; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < C)
+                v[u] = ld_stream16(xrow + (size_t)c * 8);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int p = slot_row(p0, p1, j);
+            if (p < 0)
+                continue;
+            uint16_t *dst = recv + (size_t)p * H;
 #pragma unroll
             for (int u = 0; u < kBf16Unroll; ++u) {
-                const int c = c0 + u * kDispThreads;
+                const int c = c0 + 32 * u;
                 if (c < C)
-                    v[u] = ld_stream16(xrow + (size_t)c * 8);
-            }
-            for (int j = 0; j < k; ++j) {
-                const int p = s_pos[j];
-                if (p < 0)
-                    continue;
-                uint16_t *dst = recv + (size_t)p * H;
-#pragma unroll
-                for (int u = 0; u < kBf16Unroll; ++u) {
-                    const int c = c0 + u * kDispThreads;
-                    if (c < C)
-                        st_stream16(dst + (size_t)c * 8, v[u]);
-                }
+                    st_stream16(dst + (size_t)c * 8, v[u]);
             }
         }
     }
@@ -83,80 +130,78 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16
                                                                     float *__restrict__ recv_s,
                                                                     int32_t *__restrict__ err_flag)
 {
-    __shared__ int32_t s_pos[kMaxK];
-    const int C16 = H / 16;    // 16-column groups per row; 8 per 128-column block
-    const int nb = H / 128;    // scales per row
+    const int lane = threadIdx.x & 31;
+    const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
+    const int nb = H / 128;  // scales per row
+    const int segs = (C16 + 31) / 32;
     const long long rows = (long long)T * k;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        load_rows(pos, t, k, rows, s_pos, err_flag);
-        const uint16_t *xrow = x + (size_t)t * H;
-        // The trip count is the same for every thread, so whole 8-lane
-        // groups are active or idle together and the shuffles see all lanes.
-        for (int base = 0; base < C16; base += kDispThreads) {
-            const int c = base + threadIdx.x;
-            const bool act = c < C16;
-            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-            if (act) {
-                a = ld_stream16(xrow + (size_t)c * 16);
-                b = ld_stream16(xrow + (size_t)c * 16 + 8);
-            }
-            const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float f[16];
+    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+        int p0, p1;
+        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
+        const uint16_t *xrow = x + (size_t)it.t * H;
+        const int c = it.seg * 32 + lane;
+        // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
+        const bool act = c < C16;
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (act) {
+            a = ld_stream16(xrow + (size_t)c * 16);
+            b = ld_stream16(xrow + (size_t)c * 16 + 8);
+        }
+        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float f[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = bf16_lo(wv[i]);
-                f[2 * i + 1] = bf16_hi(wv[i]);
-            }
-            float amax = 0.0f;
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = bf16_lo(wv[i]);
+            f[2 * i + 1] = bf16_hi(wv[i]);
+        }
+        float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                amax = fmaxf(amax, fabsf(f[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-            const float s = __fdiv_rn(amax, 448.0f);
-            uint32_t q[4];
-            if (amax == 0.0f) {
-                // all zeros: keep each element's sign bit (bf16 bit 15 -> code bit 7)
+        for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+        const float s = __fdiv_rn(amax, 448.0f);
+        uint32_t q[4];
+        if (amax == 0.0f) {
+            // all zeros: keep each element's sign bit (bf16 bit 15 -> code bit 7)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t w0 = wv[2 * i], w1 = wv[2 * i + 1];
-                    q[i] = ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
-                           (w1 & 0x80000000u);
-                }
-            } else {
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w0 = wv[2 * i], w1 = wv[2 * i + 1];
+                q[i] = ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
+                       (w1 & 0x80000000u);
+            }
+        } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
-                    const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
-                    q[i] = lo | (hi << 16);
-                }
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
+                const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
+                q[i] = lo | (hi << 16);
             }
-            if (act) {
-                const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-                for (int j = 0; j < k; ++j) {
-                    const int p = s_pos[j];
-                    if (p < 0)
-                        continue;
-                    st_stream16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
-                    if ((c & 7) == 0)
-                        recv_s[(size_t)p * nb + (c >> 3)] = s;
-                }
-            }
+        }
+        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+        for (int j = 0; j < k; ++j) {
+            const int p = slot_row(p0, p1, j);
+            if (p < 0 || !act)
+                continue;
+            st_stream16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
+            if ((c & 7) == 0)
+                recv_s[(size_t)p * nb + (c >> 3)] = s;
         }
     }
 }
 
-// A grid of (resident CTAs per SM) x (SMs), capped at one CTA per token.
-int dispatch_grid(const void *kernel, int &per_sm_cache, int T)
+// A persistent grid of (resident CTAs per SM) x (SMs), capped by the work.
+int persistent_grid(const void *kernel, int &per_sm_cache, long long warp_items)
 {
     if (per_sm_cache < 1) {
         int per_sm = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDispThreads, 0);
         per_sm_cache = per_sm < 1 ? 1 : per_sm;
     }
-    const int g = device_sm_count() * per_sm_cache;
-    return T < g ? T : g;
+    const long long g = (long long)device_sm_count() * per_sm_cache;
+    const long long need = (warp_items + kDispThreads / 32 - 1) / (kDispThreads / 32);
+    return (int)(need < g ? need : g);
 }
 
 int g_bf16_per_sm = 0;
@@ -169,7 +214,9 @@ cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const i
 {
     if (T == 0)
         return cudaSuccess;
-    const int grid = dispatch_grid((const void *)dispatch_bf16_kernel, g_bf16_per_sm, T);
+    const int C = H / 8;
+    const long long items = (long long)T * ((C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll));
+    const int grid = persistent_grid((const void *)dispatch_bf16_kernel, g_bf16_per_sm, items);
     dispatch_bf16_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv, err_flag);
     return cudaGetLastError();
 }
@@ -179,7 +226,8 @@ cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const in
 {
     if (T == 0)
         return cudaSuccess;
-    const int grid = dispatch_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, T);
+    const long long items = (long long)T * ((H / 16 + 31) / 32);
+    const int grid = persistent_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, items);
     dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, err_flag);
     return cudaGetLastError();
 }

@@ -37,13 +37,13 @@ constexpr int kMaxGateK = 32;
 constexpr int kMaxGroups = 32;
 constexpr int kMaxKin = 4;
 constexpr int kMaxLayoutExperts = 1024;
-constexpr int kMaxRowK = 64;
+constexpr int kMaxRowK = 64;  // slots per token accepted by layout, dispatch and combine
 
 ep_status check_layout_args(int32_t T, int32_t k, int32_t E, int32_t epr)
 {
     if (T < 0 || k < 1 || E < 1 || epr < 1 || E % epr != 0)
         return EP_ERR_INVALID_ARG;
-    if (E > kMaxLayoutExperts || (int64_t)T * k >= (int64_t)INT32_MAX)
+    if (E > kMaxLayoutExperts || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
         return EP_ERR_UNSUPPORTED;
     return EP_OK;
 }

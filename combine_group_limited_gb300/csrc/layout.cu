@@ -7,18 +7,21 @@
 // distinct experts fills at most T*k rows, so nothing here is read back to
 // the host.
 //
-// Three launches over tiles of whole tokens (about 2048 entries each):
+// Three launches over tiles of whole tokens (about 512 entries each):
 //  1. count:  per tile, per-expert entry counts and per-rank distinct-token
 //             counts (shared-memory integer atomics; the totals do not depend
-//             on their order).
-//  2. scan:   one CTA: per expert, an exclusive scan over tiles (warp scans);
-//             then an exclusive scan over experts and the per-rank sums.
-//  3. place:  per tile, the stable row of every entry: 8 warps take
-//             contiguous slices in flat order; __match_any_sync groups equal
-//             experts inside a 32-entry chunk, so an entry's rank is the
-//             popcount of lower lanes in its group plus the running count of
-//             its warp, whose base is the tile's base plus the lower warps'
-//             counts.  The result is the order a sequential walk gives.
+//             on their order).  Workspace columns [E][tiles], [R][tiles].
+//  2. scan:   one warp per column: experts get an exclusive scan over tiles
+//             (in place) and their total; ranks get their distinct-token sum.
+//  3. place:  every CTA scans the E expert totals itself (a block scan of at
+//             most 1024 values, 4 per thread) to get expert_off, then gives each entry its
+//             stable row: 8 warps take contiguous slices in flat order;
+//             __match_any_sync groups equal experts inside a 32-entry chunk,
+//             so an entry's row is its expert's offset + the tile's base + the
+//             lower warps' counts + the running count of its warp + the
+//             popcount of lower lanes in its group -- the order a sequential
+//             walk gives.  CTA 0 also writes the offsets and the per-rank
+//             arrays; all CTAs fill src past the last row with -1.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -27,8 +30,9 @@ namespace {
 
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
-constexpr int kTileEntries = 2048;
-constexpr int kScanThreads = 1024;
+constexpr int kTileEntries = 512;
+constexpr int kPlaceThreads = 256;
+constexpr int kPlaceWarps = kPlaceThreads / 32;
 constexpr int kMaxExperts = 1024;
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return (unsigned)e < (unsigned)E; }
@@ -37,41 +41,43 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(
     const int32_t *__restrict__ idx, int T, int k, int E, int epr, int tile_tok, int nt,
     int32_t *__restrict__ ws_cnt, int32_t *__restrict__ ws_rt, int32_t *__restrict__ err_flag)
 {
-    extern __shared__ int32_t cnt_smem[];  // [E] expert counts, [R] rank token counts
+    // [E] expert counts, [R] rank token counts, [kTileEntries] the tile's ranks
+    extern __shared__ int32_t cnt_smem[];
     const int R = E / epr;
+    int32_t *s_rank = cnt_smem + E + R;
     for (int i = threadIdx.x; i < E + R; i += blockDim.x)
         cnt_smem[i] = 0;
     __syncthreads();
 
     const int tile = blockIdx.x;
-    const int t0 = tile * tile_tok;
-    const int t1 = min(T, t0 + tile_tok);
+    const int n0 = tile * tile_tok * k;
+    const int n1 = min(T, (tile + 1) * tile_tok) * k;
     int bad = 0;
-    for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
         const int e = __ldg(idx + i);
-        if (valid_expert(e, E))
+        int r = -1;
+        if (valid_expert(e, E)) {
             atomicAdd(&cnt_smem[e], 1);
-        else if (e != -1)
+            r = e / epr;
+        } else if (e != -1) {
             bad = 1;
-    }
-    for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-        const int32_t *r_ = idx + (size_t)t * k;
-        for (int j = 0; j < k; ++j) {
-            const int e = __ldg(r_ + j);
-            if (!valid_expert(e, E))
-                continue;
-            const int r = e / epr;
-            bool first = true;
-            for (int jj = 0; jj < j; ++jj) {
-                const int e2 = __ldg(r_ + jj);
-                if (valid_expert(e2, E) && e2 / epr == r) {
-                    first = false;
-                    break;
-                }
-            }
-            if (first)
-                atomicAdd(&cnt_smem[E + r], 1);
         }
+        s_rank[i - n0] = r;
+    }
+    __syncthreads();
+    // Distinct tokens per rank: an entry counts if no earlier slot of its
+    // token is on the same rank.
+    for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
+        const int r = s_rank[i - n0];
+        if (r < 0)
+            continue;
+        const int j = (i - n0) % k;
+        const int32_t *tok = s_rank + (i - n0 - j);
+        bool first = true;
+        for (int jj = 0; jj < j; ++jj)
+            first &= tok[jj] != r;
+        if (first)
+            atomicAdd(&cnt_smem[E + r], 1);
     }
     if (bad && err_flag)
         atomicOr(err_flag, (int)1);
@@ -94,108 +100,130 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
     return v;
 }
 
-__global__ void __launch_bounds__(kScanThreads) layout_scan_kernel(
-    int T, int k, int E, int epr, int nt, int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ ws_rt,
-    int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_off, int32_t *__restrict__ rank_count,
-    int32_t *__restrict__ rank_off, int32_t *__restrict__ rank_tokens, int32_t *__restrict__ src)
+// One warp per column: columns [0, E) are expert columns (scanned in place,
+// total to expert_count), columns [E, E+R) are rank columns (summed into
+// rank_tokens).
+__global__ void __launch_bounds__(kLayoutThreads) layout_scan_kernel(
+    int E, int R, int nt, int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ ws_rt,
+    int32_t *__restrict__ expert_count, int32_t *__restrict__ rank_tokens)
 {
-    __shared__ int32_t s_cnt[kMaxExperts];
-    __shared__ int32_t s_wsum[kScanThreads / 32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    const int R = E / epr;
-
-    // Per expert: exclusive scan over tiles, in place; total = expert count.
-    for (int e = warp; e < E; e += nwarps) {
-        int32_t *col = ws_cnt + (size_t)e * nt;
+    const int lane = threadIdx.x & 31;
+    const int col = blockIdx.x * kLayoutWarps + (threadIdx.x >> 5);
+    if (col >= E + R)
+        return;
+    if (col < E) {
+        int32_t *c = ws_cnt + (size_t)col * nt;
         int running = 0;
-        for (int base = 0; base < nt; base += 32) {
-            const int tl = base + lane;
-            const int v = tl < nt ? col[tl] : 0;
-            const int incl = warp_incl_scan(v, lane);
-            if (tl < nt)
-                col[tl] = running + incl - v;
-            running += __shfl_sync(kFullMask, incl, 31);
+        for (int base = 0; base < nt; base += 128) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int tl = base + 32 * u + lane;
+                v[u] = tl < nt ? c[tl] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int tl = base + 32 * u + lane;
+                const int incl = warp_incl_scan(v[u], lane);
+                if (tl < nt)
+                    c[tl] = running + incl - v[u];
+                running += __shfl_sync(kFullMask, incl, 31);
+            }
         }
-        if (lane == 0) {
-            s_cnt[e] = running;
-            expert_count[e] = running;
-        }
-    }
-    // Per rank: distinct tokens summed over tiles.
-    for (int r = warp; r < R; r += nwarps) {
-        const int32_t *col = ws_rt + (size_t)r * nt;
+        if (lane == 0)
+            expert_count[col] = running;
+    } else {
+        const int r = col - E;
+        const int32_t *c = ws_rt + (size_t)r * nt;
         int acc = 0;
         for (int tl = lane; tl < nt; tl += 32)
-            acc += col[tl];
+            acc += c[tl];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             acc += __shfl_xor_sync(kFullMask, acc, off);
         if (lane == 0)
             rank_tokens[r] = acc;
     }
-    __syncthreads();
-
-    // Exclusive scan over experts (E <= 1024 = one value per thread).
-    const int e = threadIdx.x;
-    const int v = e < E ? s_cnt[e] : 0;
-    const int incl = warp_incl_scan(v, lane);
-    if (lane == 31)
-        s_wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int ws = lane < nwarps ? s_wsum[lane] : 0;
-        const int wi = warp_incl_scan(ws, lane);
-        if (lane < nwarps)
-            s_wsum[lane] = wi - ws;
-    }
-    __syncthreads();
-    const int excl = s_wsum[warp] + incl - v;
-    __syncthreads();
-    if (e < E)
-        s_cnt[e] = excl;  // reuse as offsets
-    __shared__ int32_t s_total;
-    if (e == E - 1)
-        s_total = excl + v;
-    __syncthreads();
-    const int total = s_total;
-    if (e < E)
-        expert_off[e] = excl;
-    if (e == 0)
-        expert_off[E] = total;
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-        const int lo = s_cnt[r * epr];
-        const int hi = (r + 1) * epr < E ? s_cnt[(r + 1) * epr] : total;
-        rank_off[r] = lo;
-        rank_count[r] = hi - lo;
-    }
-    if (threadIdx.x == 0)
-        rank_off[R] = total;
-    // Rows no entry lands on.
-    for (int i = total + threadIdx.x; i < T * k; i += blockDim.x)
-        src[i] = -1;
 }
 
-__global__ void __launch_bounds__(kLayoutThreads) layout_place_kernel(
-    const int32_t *__restrict__ idx, int T, int k, int E, int tile_tok, int nt, const int32_t *__restrict__ ws_cnt,
-    const int32_t *__restrict__ expert_off, int32_t *__restrict__ pos, int32_t *__restrict__ src,
-    int32_t *__restrict__ err_flag)
+__global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
+    const int32_t *__restrict__ idx, int T, int k, int E, int epr, int tile_tok, int nt,
+    const int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_off,
+    int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_off, int32_t *__restrict__ pos,
+    int32_t *__restrict__ src, int32_t *__restrict__ err_flag)
 {
-    extern __shared__ int32_t hist[];  // [kLayoutWarps][E]
+    extern __shared__ int32_t place_smem[];  // hist [kPlaceWarps][E], off [E]
+    int32_t *hist = place_smem;
+    int32_t *s_off = place_smem + kPlaceWarps * E;
+    __shared__ int32_t s_wsum[kPlaceWarps];
+    __shared__ int32_t s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
+    const int n_total = T * k;
+
+    // Expert offsets: exclusive scan of the E <= 1024 totals, kPerThread
+    // consecutive experts per thread.
+    {
+        constexpr int kPerThread = kMaxExperts / kPlaceThreads;
+        const int e0 = threadIdx.x * kPerThread;
+        int v[kPerThread];
+        int sum = 0;
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            v[u] = e0 + u < E ? __ldg(expert_count + e0 + u) : 0;
+            sum += v[u];
+        }
+        const int incl = warp_incl_scan(sum, lane);
+        if (lane == 31)
+            s_wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int ws = lane < kPlaceWarps ? s_wsum[lane] : 0;
+            const int wi = warp_incl_scan(ws, lane);
+            if (lane < kPlaceWarps)
+                s_wsum[lane] = wi - ws;
+        }
+        __syncthreads();
+        int run = s_wsum[warp] + incl - sum;
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            if (e0 + u < E)
+                s_off[e0 + u] = run;
+            if (e0 + u == E - 1)
+                s_total = run + v[u];
+            run += v[u];
+        }
+    }
+    for (int i = threadIdx.x; i < kPlaceWarps * E; i += blockDim.x)
+        hist[i] = 0;
+    __syncthreads();
+    const int total = s_total;
+    if (tile == 0) {
+        const int R = E / epr;
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            expert_off[e] = s_off[e];
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            const int lo = s_off[r * epr];
+            const int hi = (r + 1) * epr < E ? s_off[(r + 1) * epr] : total;
+            rank_off[r] = lo;
+            rank_count[r] = hi - lo;
+        }
+        if (threadIdx.x == 0) {
+            expert_off[E] = total;
+            rank_off[R] = total;
+        }
+    }
+    // Rows no entry lands on.
+    for (int i = total + blockIdx.x * blockDim.x + threadIdx.x; i < n_total; i += gridDim.x * blockDim.x)
+        src[i] = -1;
+
     const int n0 = tile * tile_tok * k;
     const int n1 = min(T, (tile + 1) * tile_tok) * k;
-    const int per_warp = (((n1 - n0) + kLayoutWarps * 32 - 1) / (kLayoutWarps * 32)) * 32;
+    const int per_warp = (((n1 - n0) + kPlaceWarps * 32 - 1) / (kPlaceWarps * 32)) * 32;
     const int w0 = n0 + warp * per_warp;
     const int w1 = min(n1, w0 + per_warp);
     int32_t *my = hist + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int n_total = T * k;
-
-    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x)
-        hist[i] = 0;
-    __syncthreads();
 
     // A: each warp's per-expert counts.
     for (int c = w0; c < w1; c += 32) {
@@ -211,8 +239,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_place_kernel(
 
     // B: warp bases = expert offset + tile base + counts of the lower warps.
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int base = __ldg(expert_off + e) + __ldg(ws_cnt + (size_t)e * nt + tile);
-        for (int w = 0; w < kLayoutWarps; ++w) {
+        int base = s_off[e] + __ldg(ws_cnt + (size_t)e * nt + tile);
+        for (int w = 0; w < kPlaceWarps; ++w) {
             const int c = hist[w * E + e];
             hist[w * E + e] = base;
             base += c;
@@ -249,6 +277,25 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_place_kernel(
     }
 }
 
+// Zero counts for an empty batch (no tile runs).
+__global__ void layout_empty_kernel(int E, int epr, int32_t *expert_count, int32_t *expert_off,
+                                    int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens)
+{
+    const int R = E / epr;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+        if (i < E)
+            expert_count[i] = 0;
+        expert_off[i] = 0;
+    }
+    for (int i = threadIdx.x; i <= R; i += blockDim.x) {
+        if (i < R) {
+            rank_count[i] = 0;
+            rank_tokens[i] = 0;
+        }
+        rank_off[i] = 0;
+    }
+}
+
 }  // namespace
 
 int layout_tile_tokens(int k)
@@ -278,18 +325,20 @@ cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr,
     const int tile_tok = layout_tile_tokens(k);
     const int nt = layout_num_tiles(T, k);
     const int R = E / epr;
+    if (nt == 0) {
+        layout_empty_kernel<<<1, 256, 0, st>>>(E, epr, expert_count, expert_off, rank_count, rank_off, rank_tokens);
+        return cudaGetLastError();
+    }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     int32_t *ws_rt = ws_cnt + (size_t)nt * E;
-    if (nt > 0) {
-        layout_count_kernel<<<nt, kLayoutThreads, (E + R) * sizeof(int32_t), st>>>(
-            topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt, ws_rt, err_flag);
-    }
-    layout_scan_kernel<<<1, kScanThreads, 0, st>>>(T, k, E, epr, nt, ws_cnt, ws_rt, expert_count, expert_off,
-                                                   rank_count, rank_off, rank_tokens, src);
-    if (nt > 0) {
-        layout_place_kernel<<<nt, kLayoutThreads, kLayoutWarps * E * sizeof(int32_t), st>>>(
-            topk_idx, T, k, E, tile_tok, nt, ws_cnt, expert_off, pos, src, err_flag);
-    }
+    layout_count_kernel<<<nt, kLayoutThreads, (E + R + kTileEntries) * sizeof(int32_t), st>>>(
+        topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt, ws_rt, err_flag);
+    const int scan_grid = (E + R + kLayoutWarps - 1) / kLayoutWarps;
+    layout_scan_kernel<<<scan_grid, kLayoutThreads, 0, st>>>(E, R, nt, ws_cnt, ws_rt, expert_count, rank_tokens);
+    const size_t place_smem = ((size_t)kPlaceWarps * E + E) * sizeof(int32_t);
+    layout_place_kernel<<<nt, kPlaceThreads, place_smem, st>>>(topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt,
+                                                               expert_count, expert_off, rank_count, rank_off, pos,
+                                                               src, err_flag);
     return cudaGetLastError();
 }
 

@@ -135,7 +135,7 @@ size_t ep_layout_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t expert
  *               bytes, 16-byte aligned; contents need no initialisation and
  *               are garbage afterwards.  It must not be shared by layouts
  *               in flight at the same time.
- * Limits: 1 <= E <= 1024, experts_per_rank divides E, k >= 1, T >= 0,
+ * Limits: 1 <= E <= 1024, experts_per_rank divides E, 1 <= k <= 64, T >= 0,
  * T*k < 2^31.  Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED,
  * EP_ERR_ALIGNMENT, EP_ERR_CUDA.
  */
@@ -158,8 +158,8 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
  * a fixed 1 MiB device array inside this library (every GPU that loads the
  * library keeps it until the process exits); sizes whose
  * ep_layout_workspace_bytes exceeds 1 MiB are rejected with
- * EP_ERR_UNSUPPORTED (for example T*k up to about 1.8 million entries at
- * E = 256, experts_per_rank = 8).  The call allocates nothing.  The first
+ * EP_ERR_UNSUPPORTED (T*k up to about 465 thousand entries fit at E = 256,
+ * experts_per_rank = 8).  The call allocates nothing.  The first
  * call on a device looks up the array's device address (with that device
  * current) and caches it: make that first call before any stream capture.
  * Every call on a device shares the one array, so calls whose work overlaps
