@@ -237,10 +237,20 @@ def run_ours(args):
     r = PathRunner(cfg, seed_offset=1000 * rank)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda").fill_(1)
+
+    def flush_l2(s):
+        # Evict the step's data from L2: write a buffer twice the L2 size,
+        # then read another one so that the written lines are back in HBM
+        # before the timed events (L2 is write-back; otherwise the next
+        # step would pay for writing the flush buffer).
+        flush.fill_(s & 0xFF)
+        flush_rd.sum()
+
     ops = ("gate", "layout", "dispatch", "combine")
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    for w in range(args.warmup):
+        flush_l2(w)
         r.step()
     torch.cuda.synchronize()
 
@@ -251,7 +261,7 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         clk.mark_start()
         for s in range(args.steps):
-            flush.fill_(s & 0xFF)                       # evict L2 between steps (outside the events)
+            flush_l2(s)                                 # evict L2 between steps (outside the events)
             ev[s][0].record(stream)
             for i, op in enumerate(ops):
                 getattr(r, op)()
@@ -312,7 +322,7 @@ def run_ours(args):
                        "n_groups": cfg["n_groups"], "topk_group": cfg["topk_group"],
                        "logical_ranks": cfg["E"] // cfg["experts_per_rank"],
                        "payload": "bf16 rows in, e4m3+fp32 1x128 scales dispatched, bf16 expert outputs combined",
-                       "l2": "flushed between steps (256 MB write outside the timed events)",
+                       "l2": "flushed between steps outside the timed events: 256 MB write, then 256 MB read",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "ops": op_summary,
             "roofline": {"bound": "hbm", "kernel": kname[dom], "achieved": op_summary[dom]["GB/s"],

@@ -18,11 +18,12 @@ LIB_PATH = os.path.join(PKG, "libep_gb300.so")
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_ALIGNMENT, EP_ERR_CUDA = range(5)
 EP_FLAG_BAD_EXPERT, EP_FLAG_BAD_ROW = 1, 2
 EP_SCORE_RAW, EP_SCORE_SOFTMAX = 0, 1
-EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128 = 0, 1
+EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128, EP_DTYPE_MXFP8_E4M3_B32 = 0, 1, 2
 
 # Symbols include/ep.h declares (checked by the CPU test suite).
 EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch",
-           "ep_combine", "ep_status_str")
+           "ep_combine", "ep_combine_fp8", "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward",
+           "ep_status_str")
 
 
 class GateCfg(ctypes.Structure):
@@ -55,9 +56,14 @@ def load():
     lib.ep_layout_workspace_bytes.restype = sz
     lib.ep_get_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]
     lib.ep_get_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
-    lib.ep_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, P, P, P]
-    lib.ep_combine.argtypes = [P, P, P, i32, i32, i32, P, P, P]
-    for f in ("ep_gate", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine"):
+    lib.ep_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, i32, P, P, P]
+    lib.ep_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P]
+    lib.ep_combine_fp8.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, P, P, P]
+    lib.ep_get_layout_capacity.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.ep_dispatch_backward.argtypes = [P, i32, P, i32, i32, i32, P, P, P]
+    lib.ep_combine_backward.argtypes = [P, P, i32, P, P, i32, i32, i32, P, P, P, P]
+    for f in ("ep_gate", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine", "ep_combine_fp8",
+              "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ep_status_str.argtypes = [ctypes.c_int]
     lib.ep_status_str.restype = ctypes.c_char_p
@@ -94,6 +100,12 @@ def _dev(t, dtype, name, shape=None):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
     return t
+
+
+def _rows_of(t, H, name):
+    if t.dim() != 2 or t.shape[1] != H:
+        raise ValueError("%s must be [rows, %d]" % (name, H))
+    return t.shape[0]
 
 
 def gate_cfg(num_experts, top_k, n_groups=1, topk_group=1, topk_in_group=1, score_fn=EP_SCORE_RAW, normalize=True):
@@ -181,10 +193,12 @@ def ep_get_layout_noalloc(topk_idx, num_experts, experts_per_rank, out, err_flag
 
 
 def ep_dispatch(x, pos, dtype="bf16", recv=None, recv_scales=None, err_flag=None, stream=None):
-    """Step 3.  x bf16 [T,H], pos int32 [T,k].
+    """Step 3.  x bf16 [T,H], pos int32 [T,k].  recv defaults to T*k rows
+    (any row count may be passed, e.g. E*capacity for a capacity layout).
 
-    dtype "bf16" -> recv bf16 [T*k, H];
-    dtype "fp8"  -> (recv uint8 e4m3 codes [T*k, H], recv_scales fp32 [T*k, H/128]).
+    dtype "bf16"  -> recv bf16 [T*k, H];
+    dtype "fp8"   -> (recv uint8 e4m3 codes [T*k, H], recv_scales fp32 [T*k, H/128]);
+    dtype "mxfp8" -> (recv uint8 e4m3 codes [T*k, H], recv_scales uint8 E8M0 [T*k, H/32]).
     """
     lib = load()
     _dev(x, torch.bfloat16, "x")
@@ -198,20 +212,28 @@ def ep_dispatch(x, pos, dtype="bf16", recv=None, recv_scales=None, err_flag=None
     if dtype == "bf16":
         if recv is None:
             recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
-        _dev(recv, torch.bfloat16, "recv", (T * k, H))
-        _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos), EP_DTYPE_BF16, _ptr(recv), None,
-                                              _ptr(err_flag), _stream(stream)))
+        _dev(recv, torch.bfloat16, "recv")
+        _rows_of(recv, H, "recv")
+        _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos), EP_DTYPE_BF16, _ptr(recv), recv.shape[0],
+                                              None, _ptr(err_flag), _stream(stream)))
         return recv
-    if dtype != "fp8":
-        raise ValueError("dtype must be 'bf16' or 'fp8'")
+    if dtype not in ("fp8", "mxfp8"):
+        raise ValueError("dtype must be 'bf16', 'fp8' or 'mxfp8'")
+    mx = dtype == "mxfp8"
     if recv is None:
         recv = torch.empty((T * k, H), dtype=torch.uint8, device=x.device)
     if recv_scales is None:
-        recv_scales = torch.empty((T * k, max(H // 128, 1)), dtype=torch.float32, device=x.device)
-    _dev(recv, torch.uint8, "recv", (T * k, H))
-    _dev(recv_scales, torch.float32, "recv_scales")
-    _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos), EP_DTYPE_FP8_E4M3_B128, _ptr(recv),
-                                          _ptr(recv_scales), _ptr(err_flag), _stream(stream)))
+        if mx:
+            recv_scales = torch.empty((T * k, max(H // 32, 1)), dtype=torch.uint8, device=x.device)
+        else:
+            recv_scales = torch.empty((T * k, max(H // 128, 1)), dtype=torch.float32, device=x.device)
+    _dev(recv, torch.uint8, "recv")
+    _rows_of(recv, H, "recv")
+    _dev(recv_scales, torch.uint8 if mx else torch.float32, "recv_scales",
+         (recv.shape[0], H // (32 if mx else 128)))
+    _check("ep_dispatch", lib.ep_dispatch(_ptr(x), T, H, k, _ptr(pos),
+                                          EP_DTYPE_MXFP8_E4M3_B32 if mx else EP_DTYPE_FP8_E4M3_B128, _ptr(recv),
+                                          recv.shape[0], _ptr(recv_scales), _ptr(err_flag), _stream(stream)))
     return recv, recv_scales
 
 
@@ -223,13 +245,101 @@ def ep_combine(y, pos, topk_w, out=None, err_flag=None, stream=None):
     T, k = pos.shape
     _dev(topk_w, torch.float32, "topk_w", (T, k))
     H = y.shape[1]
-    if y.shape[0] != T * k:
-        raise ValueError("y must have T*k rows")
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
     _dev(out, torch.bfloat16, "out", (T, H))
     if err_flag is not None:
         _dev(err_flag, torch.int32, "err_flag")
-    _check("ep_combine", lib.ep_combine(_ptr(y), _ptr(pos), _ptr(topk_w), T, H, k, _ptr(out), _ptr(err_flag),
-                                        _stream(stream)))
+    _check("ep_combine", lib.ep_combine(_ptr(y), y.shape[0], _ptr(pos), _ptr(topk_w), T, H, k, _ptr(out),
+                                        _ptr(err_flag), _stream(stream)))
     return out
+
+
+def ep_combine_fp8(yq, yscales, pos, topk_w, out=None, err_flag=None, stream=None):
+    """Steps 4-5 on FP8 expert outputs.  yq uint8 e4m3 [T*k, H]; yscales fp32
+    [T*k, H/128] (1x128) or uint8 E8M0 [T*k, H/32] (MXFP8) -> out bf16 [T,H]."""
+    lib = load()
+    _dev(yq, torch.uint8, "yq")
+    _dev(pos, torch.int32, "pos")
+    T, k = pos.shape
+    _dev(topk_w, torch.float32, "topk_w", (T, k))
+    H = yq.shape[1]
+    mx = yscales.dtype == torch.uint8
+    _dev(yscales, torch.uint8 if mx else torch.float32, "yscales")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=yq.device)
+    _dev(out, torch.bfloat16, "out", (T, H))
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _dev(yscales, torch.uint8 if mx else torch.float32, "yscales", (yq.shape[0], H // (32 if mx else 128)))
+    _check("ep_combine_fp8", lib.ep_combine_fp8(
+        _ptr(yq), _ptr(yscales), EP_DTYPE_MXFP8_E4M3_B32 if mx else EP_DTYPE_FP8_E4M3_B128, yq.shape[0], _ptr(pos),
+        _ptr(topk_w), T, H, k, _ptr(out), _ptr(err_flag), _stream(stream)))
+    return out
+
+
+CapLayout = namedtuple("CapLayout", "expert_count expert_off rank_count rank_off rank_tokens expert_dropped pos src")
+
+
+def ep_get_layout_capacity(topk_idx, num_experts, experts_per_rank, capacity, workspace=None, err_flag=None,
+                           stream=None):
+    """Capacity-limited layout: expert e owns rows [e*capacity, (e+1)*capacity)."""
+    lib = load()
+    _dev(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    E, epr = num_experts, experts_per_rank
+    if epr <= 0 or E % epr:
+        raise ValueError("experts_per_rank must divide num_experts")
+    R = E // epr
+    d = topk_idx.device
+    z = lambda *s: torch.empty(s, dtype=torch.int32, device=d)  # noqa: E731
+    out = CapLayout(z(E), z(E + 1), z(R), z(R + 1), z(R), z(E), z(T, k), z(max(E * capacity, 1)))
+    if workspace is None:
+        workspace = alloc_layout_workspace(T, k, E, epr, d)
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_get_layout_capacity", lib.ep_get_layout_capacity(
+        _ptr(topk_idx), T, k, E, epr, int(capacity), _ptr(out.expert_count), _ptr(out.expert_off),
+        _ptr(out.rank_count), _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.expert_dropped), _ptr(out.pos),
+        _ptr(out.src), _ptr(err_flag), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def ep_dispatch_backward(grad_recv, pos, out=None, err_flag=None, stream=None):
+    """grad_x[t] = bf16(sum_j grad_recv[pos[t,j]]).  grad_recv bf16 [T*k, H] -> bf16 [T, H]."""
+    lib = load()
+    _dev(grad_recv, torch.bfloat16, "grad_recv")
+    _dev(pos, torch.int32, "pos")
+    T, k = pos.shape
+    H = grad_recv.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=grad_recv.device)
+    _dev(out, torch.bfloat16, "grad_x", (T, H))
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_dispatch_backward", lib.ep_dispatch_backward(_ptr(grad_recv), grad_recv.shape[0], _ptr(pos), T, H, k,
+                                                            _ptr(out), _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def ep_combine_backward(grad_out, y, pos, topk_w, grad_y=None, grad_w=None, err_flag=None, stream=None):
+    """Returns (grad_y bf16 [T*k, H], grad_w fp32 [T, k])."""
+    lib = load()
+    _dev(grad_out, torch.bfloat16, "grad_out")
+    _dev(y, torch.bfloat16, "y")
+    _dev(pos, torch.int32, "pos")
+    T, k = pos.shape
+    H = grad_out.shape[1]
+    _dev(topk_w, torch.float32, "topk_w", (T, k))
+    if grad_y is None:
+        grad_y = torch.zeros((y.shape[0], H), dtype=torch.bfloat16, device=y.device)
+    if grad_w is None:
+        grad_w = torch.empty((T, k), dtype=torch.float32, device=y.device)
+    _dev(grad_y, torch.bfloat16, "grad_y", (y.shape[0], H))
+    _dev(grad_w, torch.float32, "grad_w", (T, k))
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_combine_backward", lib.ep_combine_backward(
+        _ptr(grad_out), _ptr(y), y.shape[0], _ptr(pos), _ptr(topk_w), T, H, k, _ptr(grad_y), _ptr(grad_w),
+        _ptr(err_flag), _stream(stream)))
+    return grad_y, grad_w

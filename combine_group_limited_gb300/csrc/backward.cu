@@ -1,0 +1,161 @@
+// backward.cu -- backward of the weighted combine.
+//
+// The combine of "Expert Parallelism (Parallelisme d'experts)", section "Le
+// pattern de communication all-to-all" (Phase 2: the expert outputs come back
+// and are summed weighted by the router scores) is out[t] = sum_j w[t,j] *
+// y[pos[t,j]].  Its gradients, for training (the setting of "DeepEP de
+// DeepSeek ...": forward and backward passes), are
+//   grad_y[pos[t,j], :] = w[t,j] * grad_out[t, :]        (a weighted dispatch)
+//   grad_w[t, j]        = <grad_out[t, :], y[pos[t,j], :]>
+// (The backward of the BF16 dispatch is the combine with unit weights; see
+// combine.cu.)
+//
+// One CTA per token at a time: each thread owns 16-byte column chunks; per
+// chunk it reads grad_out once and the k expert rows, writes the k scaled
+// rows, and keeps k partial dot products.  grad_y is rounded once to bf16:
+// the fp32 product p = w*g is corrected with its exact residual
+// fma(w, g, -p) (the FMA-based TwoProduct of Ogita, Rump and Oishi,
+// "Accurate sum and dot product", SIAM J. Sci. Comput. 2005) whenever p sits
+// exactly on a bf16 rounding midpoint, so the result is the correctly rounded
+// bf16 of the exact product (for products in the normal fp32 range).  The
+// dots are reduced in a fixed order (each thread's chunks in sequence, a warp
+// xor-tree, then the warps in order), so grad_w does not depend on timing.
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int kMaxK = 64;
+constexpr int kSlotBatch = 8;
+
+// bf16 nearest-even of the exact product w*g (see the file comment).
+__device__ __forceinline__ float exact_product_for_bf16(float w, float g)
+{
+    float p = w * g;
+    const float e = fmaf(w, g, -p);
+    uint32_t u = __float_as_uint(p);
+    if ((u & 0xFFFFu) == 0x8000u && e != 0.0f) {
+        // p is a bf16 midpoint but the true product is not: step one fp32 ulp
+        // toward the true product so that rounding picks its side.
+        const bool away = (e > 0.0f) == (p > 0.0f);
+        u = away ? u + 1u : u - 1u;
+        p = __uint_as_float(u);
+    }
+    return p;
+}
+
+__global__ void __launch_bounds__(kBwdThreads) combine_backward_kernel(
+    const uint16_t *__restrict__ grad_out, const uint16_t *__restrict__ y, const int32_t *__restrict__ pos,
+    const float *__restrict__ w, int T, int H, int k, uint16_t *__restrict__ grad_y, float *__restrict__ grad_w,
+    long long rows, int32_t *__restrict__ err_flag)
+{
+    __shared__ int32_t s_pos[kMaxK];
+    __shared__ float s_w[kMaxK];
+    __shared__ float s_part[kSlotBatch][kBwdWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int C = H / 8;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < k) {
+            int p = __ldg(pos + (size_t)t * k + threadIdx.x);
+            if (p >= rows) {
+                if (err_flag)
+                    atomicOr(err_flag, 2);
+                p = -1;
+            }
+            s_pos[threadIdx.x] = p;
+            s_w[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+        }
+        __syncthreads();
+        const uint16_t *grow = grad_out + (size_t)t * H;
+        for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+            float dot[kSlotBatch];
+#pragma unroll
+            for (int u = 0; u < kSlotBatch; ++u)
+                dot[u] = 0.0f;
+            for (int c = threadIdx.x; c < C; c += kBwdThreads) {
+                const uint4 gv = ld_stream16(grow + (size_t)c * 8);
+                const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+                float g[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    g[2 * i] = bf16_lo(gw4[i]);
+                    g[2 * i + 1] = bf16_hi(gw4[i]);
+                }
+                uint4 v[kSlotBatch];
+#pragma unroll
+                for (int u = 0; u < kSlotBatch; ++u) {
+                    const int j = j0 + u;
+                    const int p = j < k ? s_pos[j] : -1;
+                    if (p >= 0)
+                        v[u] = ld_stream16(y + (size_t)p * H + (size_t)c * 8);
+                }
+#pragma unroll
+                for (int u = 0; u < kSlotBatch; ++u) {
+                    const int j = j0 + u;
+                    const int p = j < k ? s_pos[j] : -1;
+                    if (p < 0)
+                        continue;
+                    const float wj = s_w[j];
+                    const uint32_t yv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    uint4 o;
+                    uint32_t *ov = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        dot[u] = fmaf(g[2 * i], bf16_lo(yv[i]), dot[u]);
+                        dot[u] = fmaf(g[2 * i + 1], bf16_hi(yv[i]), dot[u]);
+                        ov[i] = pack_bf16x2(exact_product_for_bf16(wj, g[2 * i]),
+                                            exact_product_for_bf16(wj, g[2 * i + 1]));
+                    }
+                    st_plain16(grad_y + (size_t)p * H + (size_t)c * 8, o);
+                }
+            }
+            // Fixed-order reduction of the batch's dots.
+#pragma unroll
+            for (int u = 0; u < kSlotBatch; ++u) {
+                float d = dot[u];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    d += __shfl_xor_sync(kFullMask, d, off);
+                if (lane == 0)
+                    s_part[u][warp] = d;
+            }
+            __syncthreads();
+            if (threadIdx.x < kSlotBatch && j0 + threadIdx.x < k) {
+                const int j = j0 + threadIdx.x;
+                float d = 0.0f;
+                for (int wi = 0; wi < kBwdWarps; ++wi)
+                    d += s_part[threadIdx.x][wi];
+                grad_w[(size_t)t * k + j] = s_pos[j] >= 0 ? d : 0.0f;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y, long long rows, const int32_t *pos,
+                                    const float *w, int T, int H, int k, uint16_t *grad_y, float *grad_w,
+                                    int32_t *err_flag, cudaStream_t st)
+{
+    if (T == 0)
+        return cudaSuccess;
+    static int per_sm = 0;
+    if (per_sm < 1) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_backward_kernel, kBwdThreads, 0);
+        if (per_sm < 1)
+            per_sm = 1;
+    }
+    int grid = device_sm_count() * per_sm;
+    if (grid > T)
+        grid = T;
+    combine_backward_kernel<<<grid, kBwdThreads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y, grad_w, rows,
+                                                          err_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

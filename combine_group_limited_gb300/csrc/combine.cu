@@ -11,6 +11,17 @@
 // 2H out per token.  A CTA takes one token at a time; a thread owns a
 // 16-byte column chunk and first issues the loads of up to 8 slots, then
 // runs their fmas in order, so eight 16-byte loads are in flight per thread.
+// With w == NULL every weight is 1: the backward of the BF16 dispatch (a
+// copy), whose source-row gradient is the sum of its copies' gradients.
+//
+// combine_fp8_kernel: the same reduction over FP8 expert outputs (e4m3 codes
+// with fp32 1x128 or E8M0 1x32 block scales).  A code converts exactly to
+// fp32 (cvt.rn.f16x2.e4m3x2, then f16 -> f32), times its block scale (exact
+// for E8M0 powers of two, one fp32 rounding for fp32 scales), then the same
+// fp32 fma chain in slot order.  2 bytes of FP8 payload per column per slot
+// instead of 2 bytes of BF16 halves the bytes the combine reads.
+#include <cuda_fp16.h>
+
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -24,13 +35,12 @@ constexpr int kSlotBatch = 8;
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *__restrict__ y,
                                                                const int32_t *__restrict__ pos,
                                                                const float *__restrict__ w, int T, int H, int k,
-                                                               uint16_t *__restrict__ out,
+                                                               uint16_t *__restrict__ out, long long rows,
                                                                int32_t *__restrict__ err_flag)
 {
     __shared__ int32_t s_pos[kMaxK];
     __shared__ float s_w[kMaxK];
     const int C = H / 8;
-    const long long rows = (long long)T * k;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
         if (threadIdx.x < k) {
@@ -41,7 +51,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *_
                 p = -1;
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+            s_w[threadIdx.x] = w ? __ldg(w + (size_t)t * k + threadIdx.x) : 1.0f;
         }
         __syncthreads();
         for (int c = threadIdx.x; c < C; c += kCombThreads) {
@@ -83,10 +93,111 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *_
     }
 }
 
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float &a, float &b, float &c, float &d)
+{
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    const __half2 p0 = *reinterpret_cast<const __half2 *>(&h0);
+    const __half2 p1 = *reinterpret_cast<const __half2 *>(&h1);
+    a = __low2float(p0);
+    b = __high2float(p0);
+    c = __low2float(p1);
+    d = __high2float(p1);
+}
+
+// E8M0 byte -> 2^(byte - 127) as fp32 (byte 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b)
+{
+    return b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// kMx: scales are E8M0 bytes per 32 columns; else fp32 per 128 columns.
+template <bool kMx>
+__global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t *__restrict__ yq,
+                                                                   const void *__restrict__ yscale,
+                                                                   const int32_t *__restrict__ pos,
+                                                                   const float *__restrict__ w, int T, int H, int k,
+                                                                   uint16_t *__restrict__ out, long long rows,
+                                                                   int32_t *__restrict__ err_flag)
+{
+    __shared__ int32_t s_pos[kMaxK];
+    __shared__ float s_w[kMaxK];
+    const int C16 = H / 16;
+    const int nb = kMx ? H / 32 : H / 128;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < k) {
+            int p = __ldg(pos + (size_t)t * k + threadIdx.x);
+            if (p >= rows) {
+                if (err_flag)
+                    atomicOr(err_flag, 2);
+                p = -1;
+            }
+            s_pos[threadIdx.x] = p;
+            s_w[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+        }
+        __syncthreads();
+        for (int c = threadIdx.x; c < C16; c += kCombThreads) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                acc[i] = 0.0f;
+            const int sb = kMx ? (c >> 1) : (c >> 3);  // this lane's scale block
+            for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+                uint4 v[kSlotBatch];
+                float sc[kSlotBatch];
+#pragma unroll
+                for (int u = 0; u < kSlotBatch; ++u) {
+                    const int j = j0 + u;
+                    const int p = j < k ? s_pos[j] : -1;
+                    if (p >= 0) {
+                        v[u] = ld_stream16(yq + (size_t)p * H + (size_t)c * 16);
+                        sc[u] = kMx ? e8m0_to_f32(__ldg(static_cast<const uint8_t *>(yscale) + (size_t)p * nb + sb))
+                                    : __ldg(static_cast<const float *>(yscale) + (size_t)p * nb + sb);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kSlotBatch; ++u) {
+                    const int j = j0 + u;
+                    const int p = j < k ? s_pos[j] : -1;
+                    if (p >= 0) {
+                        const float wj = s_w[j];
+                        const uint32_t vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float d0, d1, d2, d3;
+                            e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
+                            acc[4 * i] = fmaf(wj, d0 * sc[u], acc[4 * i]);
+                            acc[4 * i + 1] = fmaf(wj, d1 * sc[u], acc[4 * i + 1]);
+                            acc[4 * i + 2] = fmaf(wj, d2 * sc[u], acc[4 * i + 2]);
+                            acc[4 * i + 3] = fmaf(wj, d3 * sc[u], acc[4 * i + 3]);
+                        }
+                    }
+                }
+            }
+            uint4 o0, o1;
+            o0.x = pack_bf16x2(acc[0], acc[1]);
+            o0.y = pack_bf16x2(acc[2], acc[3]);
+            o0.z = pack_bf16x2(acc[4], acc[5]);
+            o0.w = pack_bf16x2(acc[6], acc[7]);
+            o1.x = pack_bf16x2(acc[8], acc[9]);
+            o1.y = pack_bf16x2(acc[10], acc[11]);
+            o1.z = pack_bf16x2(acc[12], acc[13]);
+            o1.w = pack_bf16x2(acc[14], acc[15]);
+            uint16_t *dst = out + (size_t)t * H + (size_t)c * 16;
+            st_stream16(dst, o0);
+            st_stream16(dst + 8, o1);
+        }
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t *y, const int32_t *pos, const float *w, int T, int H, int k,
-                           uint16_t *out, int32_t *err_flag, cudaStream_t st)
+cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos, const float *w, int T, int H,
+                           int k, uint16_t *out, int32_t *err_flag, cudaStream_t st)
 {
     if (T == 0)
         return cudaSuccess;
@@ -99,7 +210,34 @@ cudaError_t launch_combine(const uint16_t *y, const int32_t *pos, const float *w
     int grid = device_sm_count() * per_sm;
     if (grid > T)
         grid = T;
-    combine_kernel<<<grid, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, err_flag);
+    combine_kernel<<<grid, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace ep
+
+namespace ep {
+
+cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, long long rows, const int32_t *pos,
+                               const float *w, int T, int H, int k, uint16_t *out, int32_t *err_flag, cudaStream_t st)
+{
+    if (T == 0)
+        return cudaSuccess;
+    static int per_sm_cache[2] = {0, 0};
+    const void *kern = mx ? (const void *)combine_fp8_kernel<true> : (const void *)combine_fp8_kernel<false>;
+    int &per_sm = per_sm_cache[mx ? 1 : 0];
+    if (per_sm < 1) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombThreads, 0);
+        if (per_sm < 1)
+            per_sm = 1;
+    }
+    int grid = device_sm_count() * per_sm;
+    if (grid > T)
+        grid = T;
+    if (mx)
+        combine_fp8_kernel<true><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows, err_flag);
+    else
+        combine_fp8_kernel<false><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows, err_flag);
     return cudaGetLastError();
 }
 

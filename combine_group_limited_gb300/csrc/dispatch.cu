@@ -1,5 +1,6 @@
 // dispatch.cu -- step 3: permute-scatter of token rows into the receive
-// buffer, BF16 copy or FP8 e4m3 with one fp32 scale per 128 columns.
+// buffer, BF16 copy, FP8 e4m3 with one fp32 scale per 128 columns, or MXFP8
+// (e4m3 with one power-of-two E8M0 scale per 32 columns).
 //
 // "Expert Parallelism (Parallelisme d'experts)", section "Le pattern de
 // communication all-to-all", Phase 1 Dispatch: each token goes to the
@@ -12,8 +13,8 @@
 // grid-stride to a persistent grid of (resident CTAs per SM) x (SMs).  There
 // is no block barrier: lane j of the warp holds the token's j-th receive row
 // (and lane j of a second register slot j+32) and shuffles it to the others,
-// so every warp streams independently.  Loads bypass L1; stores carry the
-// streaming hint.  The row is held in registers and never re-read per copy.
+// so every warp streams independently.  Loads bypass L1; stores are plain.
+// The row is held in registers and never re-read per copy.
 // FP8: 8 consecutive lanes own one 128-column block (16 columns each); the
 // block's amax is a 3-step xor-shuffle max, the scale an IEEE fp32 division
 // by 448, each code an IEEE fp32 division then a round-to-nearest-even
@@ -90,13 +91,12 @@ struct ItemWalk {
 
 __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                                      int k, const int32_t *__restrict__ pos,
-                                                                     uint16_t *__restrict__ recv,
+                                                                     uint16_t *__restrict__ recv, long long rows,
                                                                      int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
     const int C = H / 8;  // 16-byte chunks per row
     const int segs = (C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll);
-    const long long rows = (long long)T * k;
     for (ItemWalk it(T, segs); it.valid(); it.next()) {
         int p0, p1;
         token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint1
             for (int u = 0; u < kBf16Unroll; ++u) {
                 const int c = c0 + 32 * u;
                 if (c < C)
-                    st_stream16(dst + (size_t)c * 8, v[u]);
+                    st_plain16(dst + (size_t)c * 8, v[u]);
             }
         }
     }
@@ -127,14 +127,13 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint1
 __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                                     int k, const int32_t *__restrict__ pos,
                                                                     uint8_t *__restrict__ recv_q,
-                                                                    float *__restrict__ recv_s,
+                                                                    float *__restrict__ recv_s, long long rows,
                                                                     int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
     const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
     const int nb = H / 128;  // scales per row
     const int segs = (C16 + 31) / 32;
-    const long long rows = (long long)T * k;
     for (ItemWalk it(T, segs); it.valid(); it.next()) {
         int p0, p1;
         token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
@@ -184,9 +183,74 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16
             const int p = slot_row(p0, p1, j);
             if (p < 0 || !act)
                 continue;
-            st_stream16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
+            st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
             if ((c & 7) == 0)
                 recv_s[(size_t)p * nb + (c >> 3)] = s;
+        }
+    }
+}
+
+// MXFP8 (OCP Microscaling v1.0, E4M3 elements): a 32-column block is two
+// lanes of 16 columns.  Its scale is 2^e, e = floor(log2(amax)) - 8 (the
+// exponent of 448) clamped to [-127, 127] and stored as the E8M0 byte e + 127
+// (amax = 0 gives e = -127).  x * 2^-e is exact in fp32 (a power-of-two
+// product; only values far below the smallest e4m3 subnormal can round, and
+// they code to a signed zero either way), then cvt.rn.satfinite to e4m3.
+__global__ void __launch_bounds__(kDispThreads) dispatch_mxfp8_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                                      int k, const int32_t *__restrict__ pos,
+                                                                      uint8_t *__restrict__ recv_q,
+                                                                      uint8_t *__restrict__ recv_e, long long rows,
+                                                                      int32_t *__restrict__ err_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const int C16 = H / 16;  // 16-column groups per row; 2 per 32-column block
+    const int nb = H / 32;   // scale bytes per row
+    const int segs = (C16 + 31) / 32;
+    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+        int p0, p1;
+        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
+        const uint16_t *xrow = x + (size_t)it.t * H;
+        const int c = it.seg * 32 + lane;
+        const bool act = c < C16;  // C16 is even: lane pairs are wholly in or out
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (act) {
+            a = ld_stream16(xrow + (size_t)c * 16);
+            b = ld_stream16(xrow + (size_t)c * 16 + 8);
+        }
+        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = bf16_lo(wv[i]);
+            f[2 * i + 1] = bf16_hi(wv[i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        // floor(log2(amax)) from the exponent field; zero and fp32 subnormals
+        // (below 2^-126) land on the clamp -127.
+        const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+        int e = ef == 0 ? -127 : ef - 127 - 8;
+        e = e < -127 ? -127 : e;
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e in [-127, 119]
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = pack_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+            const uint32_t hi = pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+            q[i] = lo | (hi << 16);
+        }
+        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+        const uint8_t eb = (uint8_t)(e + 127);
+        for (int j = 0; j < k; ++j) {
+            const int p = slot_row(p0, p1, j);
+            if (p < 0 || !act)
+                continue;
+            st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
+            if ((c & 1) == 0)
+                recv_e[(size_t)p * nb + (c >> 1)] = eb;
         }
     }
 }
@@ -206,29 +270,41 @@ int persistent_grid(const void *kernel, int &per_sm_cache, long long warp_items)
 
 int g_bf16_per_sm = 0;
 int g_fp8_per_sm = 0;
+int g_mx_per_sm = 0;
 
 }  // namespace
 
+cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const int32_t *pos, uint8_t *recv_q,
+                                  uint8_t *recv_e, long long rows, int32_t *err_flag, cudaStream_t st)
+{
+    if (T == 0)
+        return cudaSuccess;
+    const long long items = (long long)T * ((H / 16 + 31) / 32);
+    const int grid = persistent_grid((const void *)dispatch_mxfp8_kernel, g_mx_per_sm, items);
+    dispatch_mxfp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const int32_t *pos, uint16_t *recv,
-                                 int32_t *err_flag, cudaStream_t st)
+                                 long long rows, int32_t *err_flag, cudaStream_t st)
 {
     if (T == 0)
         return cudaSuccess;
     const int C = H / 8;
     const long long items = (long long)T * ((C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll));
     const int grid = persistent_grid((const void *)dispatch_bf16_kernel, g_bf16_per_sm, items);
-    dispatch_bf16_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv, err_flag);
+    dispatch_bf16_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv, rows, err_flag);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const int32_t *pos, uint8_t *recv_q,
-                                float *recv_s, int32_t *err_flag, cudaStream_t st)
+                                float *recv_s, long long rows, int32_t *err_flag, cudaStream_t st)
 {
     if (T == 0)
         return cudaSuccess;
     const long long items = (long long)T * ((H / 16 + 31) / 32);
     const int grid = persistent_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, items);
-    dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, err_flag);
+    dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag);
     return cudaGetLastError();
 }
 

@@ -131,47 +131,143 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
 }
 
 ep_status ep_dispatch(const void *x, int32_t T, int32_t H, int32_t k, const int32_t *pos, int32_t dtype, void *recv,
-                      float *recv_scales, int32_t *err_flag, void *stream)
+                      int32_t recv_rows, void *recv_scales, int32_t *err_flag, void *stream)
 {
-    if (T < 0 || H < 1 || k < 1)
+    if (T < 0 || H < 1 || k < 1 || recv_rows < 0)
         return EP_ERR_INVALID_ARG;
-    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128)
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128 && dtype != EP_DTYPE_MXFP8_E4M3_B32)
         return EP_ERR_INVALID_ARG;
     if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
         return EP_ERR_UNSUPPORTED;
-    if (dtype == EP_DTYPE_FP8_E4M3_B128 && H % 128 != 0)
+    if ((dtype == EP_DTYPE_FP8_E4M3_B128 && H % 128 != 0) || (dtype == EP_DTYPE_MXFP8_E4M3_B32 && H % 32 != 0))
         return EP_ERR_UNSUPPORTED;
     if (T == 0)
         return EP_OK;
-    if (!x || !pos || !recv || (dtype == EP_DTYPE_FP8_E4M3_B128 && !recv_scales))
+    if (!x || !pos || (recv_rows > 0 && (!recv || (dtype != EP_DTYPE_BF16 && !recv_scales))))
         return EP_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(pos, 4) || (recv_scales && !aligned(recv_scales, 4)) ||
-        (err_flag && !aligned(err_flag, 4)))
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(pos, 4) ||
+        (dtype == EP_DTYPE_FP8_E4M3_B128 && !aligned(recv_scales, 4)) || (err_flag && !aligned(err_flag, 4)))
         return EP_ERR_ALIGNMENT;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *xs = static_cast<const uint16_t *>(x);
     if (dtype == EP_DTYPE_BF16)
-        return launched(ep::launch_dispatch_bf16(static_cast<const uint16_t *>(x), T, H, k, pos,
-                                                 static_cast<uint16_t *>(recv), err_flag, st));
-    return launched(ep::launch_dispatch_fp8(static_cast<const uint16_t *>(x), T, H, k, pos,
-                                            static_cast<uint8_t *>(recv), recv_scales, err_flag, st));
+        return launched(
+            ep::launch_dispatch_bf16(xs, T, H, k, pos, static_cast<uint16_t *>(recv), recv_rows, err_flag, st));
+    if (dtype == EP_DTYPE_FP8_E4M3_B128)
+        return launched(ep::launch_dispatch_fp8(xs, T, H, k, pos, static_cast<uint8_t *>(recv),
+                                                static_cast<float *>(recv_scales), recv_rows, err_flag, st));
+    return launched(ep::launch_dispatch_mxfp8(xs, T, H, k, pos, static_cast<uint8_t *>(recv),
+                                              static_cast<uint8_t *>(recv_scales), recv_rows, err_flag, st));
 }
 
-ep_status ep_combine(const void *y, const int32_t *pos, const float *topk_w, int32_t T, int32_t H, int32_t k,
-                     void *out, int32_t *err_flag, void *stream)
+ep_status ep_combine(const void *y, int32_t y_rows, const int32_t *pos, const float *topk_w, int32_t T, int32_t H,
+                     int32_t k, void *out, int32_t *err_flag, void *stream)
 {
-    if (T < 0 || H < 1 || k < 1)
+    if (T < 0 || H < 1 || k < 1 || y_rows < 0)
         return EP_ERR_INVALID_ARG;
     if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
         return EP_ERR_UNSUPPORTED;
     if (T == 0)
         return EP_OK;
-    if (!y || !pos || !topk_w || !out)
+    if ((y_rows > 0 && !y) || !pos || !topk_w || !out)
         return EP_ERR_INVALID_ARG;
     if (!aligned(y, 16) || !aligned(out, 16) || !aligned(pos, 4) || !aligned(topk_w, 4) ||
         (err_flag && !aligned(err_flag, 4)))
         return EP_ERR_ALIGNMENT;
-    return launched(ep::launch_combine(static_cast<const uint16_t *>(y), pos, topk_w, T, H, k,
+    return launched(ep::launch_combine(static_cast<const uint16_t *>(y), y_rows, pos, topk_w, T, H, k,
                                        static_cast<uint16_t *>(out), err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_combine_fp8(const void *yq, const void *yscales, int32_t scale_dtype, int32_t y_rows, const int32_t *pos,
+                         const float *topk_w, int32_t T, int32_t H, int32_t k, void *out, int32_t *err_flag,
+                         void *stream)
+{
+    if (T < 0 || H < 1 || k < 1 || y_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    if (scale_dtype != EP_DTYPE_FP8_E4M3_B128 && scale_dtype != EP_DTYPE_MXFP8_E4M3_B32)
+        return EP_ERR_INVALID_ARG;
+    const int bs = scale_dtype == EP_DTYPE_FP8_E4M3_B128 ? 128 : 32;
+    if (H % bs != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if ((y_rows > 0 && (!yq || !yscales)) || !pos || !topk_w || !out)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(yq, 16) || !aligned(out, 16) || !aligned(pos, 4) || !aligned(topk_w, 4) ||
+        (bs == 128 && !aligned(yscales, 4)) || (err_flag && !aligned(err_flag, 4)))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_combine_fp8(static_cast<const uint8_t *>(yq), yscales, bs == 32 ? 1 : 0, y_rows, pos,
+                                           topk_w, T, H, k, static_cast<uint16_t *>(out), err_flag,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_get_layout_capacity(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E, int32_t experts_per_rank,
+                                 int32_t capacity, int32_t *expert_count, int32_t *expert_off, int32_t *rank_count,
+                                 int32_t *rank_off, int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos,
+                                 int32_t *src, int32_t *err_flag, void *workspace, size_t workspace_bytes,
+                                 void *stream)
+{
+    const ep_status a = check_layout_args(T, k, E, experts_per_rank);
+    if (a != EP_OK)
+        return a;
+    if (capacity < 0)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E * capacity >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (!expert_count || !expert_off || !rank_count || !rank_off || !rank_tokens || !expert_dropped || !workspace)
+        return EP_ERR_INVALID_ARG;
+    if ((T > 0 && (!topk_idx || !pos)) || ((int64_t)E * capacity > 0 && !src))
+        return EP_ERR_INVALID_ARG;
+    if (workspace_bytes < ep::layout_workspace_bytes(T, k, E, experts_per_rank))
+        return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {topk_idx, expert_count, expert_off, rank_count, rank_off, rank_tokens, expert_dropped,
+                          pos,      src,          err_flag};
+    for (const void *q : ptrs)
+        if (q && !aligned(q, 4))
+            return EP_ERR_ALIGNMENT;
+    if (!aligned(workspace, 16))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_layout_capacity(topk_idx, T, k, E, experts_per_rank, capacity, expert_count,
+                                               expert_off, rank_count, rank_off, rank_tokens, expert_dropped, pos,
+                                               src, err_flag, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_dispatch_backward(const void *grad_recv, int32_t recv_rows, const int32_t *pos, int32_t T, int32_t H,
+                               int32_t k, void *grad_x, int32_t *err_flag, void *stream)
+{
+    if (T < 0 || H < 1 || k < 1 || recv_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if ((recv_rows > 0 && !grad_recv) || !pos || !grad_x)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(grad_recv, 16) || !aligned(grad_x, 16) || !aligned(pos, 4) || (err_flag && !aligned(err_flag, 4)))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_combine(static_cast<const uint16_t *>(grad_recv), recv_rows, pos, nullptr, T, H, k,
+                                       static_cast<uint16_t *>(grad_x), err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_rows, const int32_t *pos,
+                              const float *topk_w, int32_t T, int32_t H, int32_t k, void *grad_y, float *grad_w,
+                              int32_t *err_flag, void *stream)
+{
+    if (T < 0 || H < 1 || k < 1 || y_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0 || k > kMaxRowK || (int64_t)T * k >= (int64_t)INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0)
+        return EP_OK;
+    if (!grad_out || (y_rows > 0 && (!y || !grad_y)) || !pos || !topk_w || !grad_w)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(grad_out, 16) || !aligned(y, 16) || !aligned(grad_y, 16) || !aligned(pos, 4) ||
+        !aligned(topk_w, 4) || !aligned(grad_w, 4) || (err_flag && !aligned(err_flag, 4)))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_combine_backward(static_cast<const uint16_t *>(grad_out),
+                                                static_cast<const uint16_t *>(y), y_rows, pos, topk_w, T, H, k,
+                                                static_cast<uint16_t *>(grad_y), grad_w, err_flag,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -60,6 +60,16 @@ __device__ __forceinline__ void st_stream16(void *p, uint4 v)
                  : "memory");
 }
 
+// Plain 16-byte global store (default L2 policy).  Measured on GB300 it is
+// slightly faster than the streaming hint for the k-fold scatter stores of
+// the dispatch, whose rows are completed by neighbouring warps while still
+// in L2.
+__device__ __forceinline__ void st_plain16(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 struct GateParams {
     int E, k, G, Kg, kin, score_fn, normalize;
 };
@@ -76,13 +86,29 @@ cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr,
                           int32_t *rank_tokens, int32_t *pos, int32_t *src, int32_t *err_flag,
                           void *workspace, cudaStream_t st);
 
-cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const int32_t *pos,
-                                 uint16_t *recv, int32_t *err_flag, cudaStream_t st);
-cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const int32_t *pos,
-                                uint8_t *recv_q, float *recv_s, int32_t *err_flag, cudaStream_t st);
+cudaError_t launch_layout_capacity(const int32_t *topk_idx, int T, int k, int E, int epr, int cap,
+                                   int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                                   int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos, int32_t *src,
+                                   int32_t *err_flag, void *workspace, cudaStream_t st);
 
-cudaError_t launch_combine(const uint16_t *y, const int32_t *pos, const float *w, int T, int H, int k,
-                           uint16_t *out, int32_t *err_flag, cudaStream_t st);
+// rows: receive-buffer rows; a pos at or past it is skipped and flagged.
+cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const int32_t *pos,
+                                 uint16_t *recv, long long rows, int32_t *err_flag, cudaStream_t st);
+cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const int32_t *pos,
+                                uint8_t *recv_q, float *recv_s, long long rows, int32_t *err_flag, cudaStream_t st);
+
+cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const int32_t *pos, uint8_t *recv_q,
+                                  uint8_t *recv_e, long long rows, int32_t *err_flag, cudaStream_t st);
+
+// w == NULL: unit weights (the backward of the BF16 dispatch).
+cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos, const float *w, int T, int H,
+                           int k, uint16_t *out, int32_t *err_flag, cudaStream_t st);
+cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, long long rows, const int32_t *pos,
+                               const float *w, int T, int H, int k, uint16_t *out, int32_t *err_flag, cudaStream_t st);
+
+cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y, long long rows, const int32_t *pos,
+                                    const float *w, int T, int H, int k, uint16_t *grad_y, float *grad_w,
+                                    int32_t *err_flag, cudaStream_t st);
 
 int device_sm_count();
 

@@ -104,7 +104,7 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 // total to expert_count), columns [E, E+R) are rank columns (summed into
 // rank_tokens).
 __global__ void __launch_bounds__(kLayoutThreads) layout_scan_kernel(
-    int E, int R, int nt, int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ ws_rt,
+    int E, int R, int nt, int zero_rank_tokens, int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ ws_rt,
     int32_t *__restrict__ expert_count, int32_t *__restrict__ rank_tokens)
 {
     const int lane = threadIdx.x & 31;
@@ -142,28 +142,45 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_scan_kernel(
         for (int off = 16; off > 0; off >>= 1)
             acc += __shfl_xor_sync(kFullMask, acc, off);
         if (lane == 0)
-            rank_tokens[r] = acc;
+            rank_tokens[r] = zero_rank_tokens ? 0 : acc;
     }
 }
 
+// kCap: capacity mode -- expert e owns the fixed rows [e*cap, (e+1)*cap); an
+// entry whose stable rank within its expert is >= cap is dropped (pos = -1).
+template <bool kCap>
 __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
-    const int32_t *__restrict__ idx, int T, int k, int E, int epr, int tile_tok, int nt,
-    const int32_t *__restrict__ ws_cnt, const int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_off,
-    int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_off, int32_t *__restrict__ pos,
-    int32_t *__restrict__ src, int32_t *__restrict__ err_flag)
+    const int32_t *__restrict__ idx, int T, int k, int E, int epr, int tile_tok, int nt, int cap,
+    const int32_t *__restrict__ ws_cnt, int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_off,
+    int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_off, int32_t *__restrict__ rank_tokens,
+    int32_t *__restrict__ expert_dropped, int32_t *__restrict__ pos, int32_t *__restrict__ src,
+    int32_t *__restrict__ err_flag)
 {
-    extern __shared__ int32_t place_smem[];  // hist [kPlaceWarps][E], off [E]
+    // hist [kPlaceWarps][E], off [E]; capacity mode adds kept ranks
+    // [kTileEntries] and kept distinct-token counts [R]
+    extern __shared__ int32_t place_smem[];
     int32_t *hist = place_smem;
     int32_t *s_off = place_smem + kPlaceWarps * E;
+    int32_t *s_krank = s_off + E;
+    int32_t *s_rt = s_krank + kTileEntries;
     __shared__ int32_t s_wsum[kPlaceWarps];
     __shared__ int32_t s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
+    const int R = E / epr;
     const int n_total = T * k;
+    const int n_rows = kCap ? E * cap : n_total;
 
-    // Expert offsets: exclusive scan of the E <= 1024 totals, kPerThread
-    // consecutive experts per thread.
-    {
+    if (kCap) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            s_off[e] = e * cap;
+        for (int r = threadIdx.x; r < R; r += blockDim.x)
+            s_rt[r] = 0;
+        if (threadIdx.x == 0)
+            s_total = E * cap;
+    } else {
+        // Expert offsets: exclusive scan of the E <= 1024 totals, kPerThread
+        // consecutive experts per thread.
         constexpr int kPerThread = kMaxExperts / kPlaceThreads;
         const int e0 = threadIdx.x * kPerThread;
         int v[kPerThread];
@@ -198,8 +215,32 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
         hist[i] = 0;
     __syncthreads();
     const int total = s_total;
-    if (tile == 0) {
-        const int R = E / epr;
+    if (tile == 0 && kCap) {
+        // The scan left each expert's total entries in expert_count; keep
+        // at most cap of them.  s_off is free for the kept counts here.
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int all = expert_count[e];
+            const int kept = all < cap ? all : cap;
+            s_off[e] = kept;
+            expert_dropped[e] = all - kept;
+            expert_off[e] = e * cap;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            expert_count[e] = s_off[e];
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            int c = 0;
+            for (int e = r * epr; e < (r + 1) * epr; ++e)
+                c += s_off[e];
+            rank_count[r] = c;
+            rank_off[r] = r * epr * cap;
+        }
+        if (threadIdx.x == 0) {
+            expert_off[E] = E * cap;
+            rank_off[R] = R * epr * cap;
+        }
+    } else if (tile == 0) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             expert_off[e] = s_off[e];
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
@@ -213,9 +254,10 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
             rank_off[R] = total;
         }
     }
-    // Rows no entry lands on.
-    for (int i = total + blockIdx.x * blockDim.x + threadIdx.x; i < n_total; i += gridDim.x * blockDim.x)
-        src[i] = -1;
+    // Rows no entry lands on (capacity mode: the launcher cleared src).
+    if (!kCap)
+        for (int i = total + blockIdx.x * blockDim.x + threadIdx.x; i < n_total; i += gridDim.x * blockDim.x)
+            src[i] = -1;
 
     const int n0 = tile * tile_tok * k;
     const int n1 = min(T, (tile + 1) * tile_tok) * k;
@@ -237,9 +279,10 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
     }
     __syncthreads();
 
-    // B: warp bases = expert offset + tile base + counts of the lower warps.
+    // B: warp bases = tile base within the expert + counts of the lower warps
+    // (+ the expert's offset outside capacity mode).
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int base = s_off[e] + __ldg(ws_cnt + (size_t)e * nt + tile);
+        int base = (kCap ? 0 : s_off[e]) + __ldg(ws_cnt + (size_t)e * nt + tile);
         for (int w = 0; w < kPlaceWarps; ++w) {
             const int c = hist[w * E + e];
             hist[w * E + e] = base;
@@ -255,44 +298,77 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
         const int e = in ? __ldg(idx + i) : -1;
         const int key = valid_expert(e, E) ? e : E;
         const unsigned grp = __match_any_sync(kFullMask, key);
+        int kept_rank = -1;
         if (key < E) {
-            const int p = my[key] + __popc(grp & lt_mask);
-            // p < T*k by construction; checked so that an index tensor
-            // changed between the launches cannot send a store astray.
-            if (p >= 0 && p < n_total) {
+            const int r = my[key] + __popc(grp & lt_mask);
+            // In capacity mode r is the rank within the expert; otherwise the
+            // row.  Rows stay below the row count by construction; checked so
+            // that an index tensor changed between the launches cannot send a
+            // store astray.
+            const int p = kCap ? (r < cap ? e * cap + r : -1) : r;
+            if (p >= 0 && p < n_rows) {
                 pos[i] = p;
                 src[p] = i;
+                kept_rank = e / epr;
             } else {
                 pos[i] = -1;
-                if (err_flag)
+                if (!kCap && err_flag)
                     atomicOr(err_flag, 2);
             }
         } else if (in) {
             pos[i] = -1;
         }
+        if (kCap && in)
+            s_krank[i - n0] = kept_rank;
         __syncwarp();
         if (key < E && lane == __ffs(grp) - 1)
             my[key] += __popc(grp);
         __syncwarp();
     }
+
+    if (kCap) {
+        // Distinct tokens with a kept entry, per rank.
+        __syncthreads();
+        for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
+            const int r = s_krank[i - n0];
+            if (r < 0)
+                continue;
+            const int j = (i - n0) % k;
+            const int32_t *tok = s_krank + (i - n0 - j);
+            bool first = true;
+            for (int jj = 0; jj < j; ++jj)
+                first &= tok[jj] != r;
+            if (first)
+                atomicAdd(&s_rt[r], 1);
+        }
+        __syncthreads();
+        for (int r = threadIdx.x; r < R; r += blockDim.x)
+            if (s_rt[r])
+                atomicAdd(rank_tokens + r, s_rt[r]);
+    }
 }
 
 // Zero counts for an empty batch (no tile runs).
-__global__ void layout_empty_kernel(int E, int epr, int32_t *expert_count, int32_t *expert_off,
-                                    int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens)
+__global__ void layout_empty_kernel(int E, int epr, int cap, int32_t *expert_count, int32_t *expert_off,
+                                    int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                                    int32_t *expert_dropped)
 {
     const int R = E / epr;
+    const int c = cap < 0 ? 0 : cap;  // capacity mode keeps its fixed offsets
     for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-        if (i < E)
+        if (i < E) {
             expert_count[i] = 0;
-        expert_off[i] = 0;
+            if (expert_dropped)
+                expert_dropped[i] = 0;
+        }
+        expert_off[i] = i * c;
     }
     for (int i = threadIdx.x; i <= R; i += blockDim.x) {
         if (i < R) {
             rank_count[i] = 0;
             rank_tokens[i] = 0;
         }
-        rank_off[i] = 0;
+        rank_off[i] = i * epr * c;
     }
 }
 
@@ -318,15 +394,23 @@ size_t layout_workspace_bytes(int T, int k, int E, int epr)
     return ((bytes + 255) / 256) * 256 + 256;
 }
 
-cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr, int32_t *expert_count,
-                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
-                          int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st)
+cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int epr, int cap,
+                               int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                               int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos, int32_t *src,
+                               int32_t *err_flag, void *workspace, cudaStream_t st)
 {
+    const bool capped = cap >= 0;
     const int tile_tok = layout_tile_tokens(k);
     const int nt = layout_num_tiles(T, k);
     const int R = E / epr;
+    if (capped && (size_t)E * cap > 0) {
+        cudaError_t e = cudaMemsetAsync(src, 0xFF, (size_t)E * cap * sizeof(int32_t), st);  // -1
+        if (e != cudaSuccess)
+            return e;
+    }
     if (nt == 0) {
-        layout_empty_kernel<<<1, 256, 0, st>>>(E, epr, expert_count, expert_off, rank_count, rank_off, rank_tokens);
+        layout_empty_kernel<<<1, 256, 0, st>>>(E, epr, cap, expert_count, expert_off, rank_count, rank_off,
+                                               rank_tokens, expert_dropped);
         return cudaGetLastError();
     }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
@@ -334,12 +418,36 @@ cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr,
     layout_count_kernel<<<nt, kLayoutThreads, (E + R + kTileEntries) * sizeof(int32_t), st>>>(
         topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt, ws_rt, err_flag);
     const int scan_grid = (E + R + kLayoutWarps - 1) / kLayoutWarps;
-    layout_scan_kernel<<<scan_grid, kLayoutThreads, 0, st>>>(E, R, nt, ws_cnt, ws_rt, expert_count, rank_tokens);
-    const size_t place_smem = ((size_t)kPlaceWarps * E + E) * sizeof(int32_t);
-    layout_place_kernel<<<nt, kPlaceThreads, place_smem, st>>>(topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt,
-                                                               expert_count, expert_off, rank_count, rank_off, pos,
-                                                               src, err_flag);
+    layout_scan_kernel<<<scan_grid, kLayoutThreads, 0, st>>>(E, R, nt, capped ? 1 : 0, ws_cnt, ws_rt, expert_count,
+                                                             rank_tokens);
+    const size_t place_smem =
+        ((size_t)kPlaceWarps * E + E + (capped ? (size_t)kTileEntries + R : 0)) * sizeof(int32_t);
+    if (capped)
+        layout_place_kernel<true><<<nt, kPlaceThreads, place_smem, st>>>(
+            topk_idx, T, k, E, epr, tile_tok, nt, cap, ws_cnt, expert_count, expert_off, rank_count, rank_off,
+            rank_tokens, expert_dropped, pos, src, err_flag);
+    else
+        layout_place_kernel<false><<<nt, kPlaceThreads, place_smem, st>>>(
+            topk_idx, T, k, E, epr, tile_tok, nt, 0, ws_cnt, expert_count, expert_off, rank_count, rank_off,
+            rank_tokens, expert_dropped, pos, src, err_flag);
     return cudaGetLastError();
+}
+
+cudaError_t launch_layout(const int32_t *topk_idx, int T, int k, int E, int epr, int32_t *expert_count,
+                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                          int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st)
+{
+    return launch_layout_impl(topk_idx, T, k, E, epr, -1, expert_count, expert_off, rank_count, rank_off,
+                              rank_tokens, nullptr, pos, src, err_flag, workspace, st);
+}
+
+cudaError_t launch_layout_capacity(const int32_t *topk_idx, int T, int k, int E, int epr, int cap,
+                                   int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                                   int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos, int32_t *src,
+                                   int32_t *err_flag, void *workspace, cudaStream_t st)
+{
+    return launch_layout_impl(topk_idx, T, k, E, epr, cap, expert_count, expert_off, rank_count, rank_off,
+                              rank_tokens, expert_dropped, pos, src, err_flag, workspace, st);
 }
 
 }  // namespace ep

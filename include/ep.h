@@ -36,11 +36,13 @@
  *  - Problems only the device can see never trap: the offending entry is
  *    skipped and a bit is OR-ed into *err_flag (a device int32, may be NULL):
  *      EP_FLAG_BAD_EXPERT  an expert index neither -1 nor in [0, E)
- *      EP_FLAG_BAD_ROW     a receive row outside [0, T*k)
+ *      EP_FLAG_BAD_ROW     a receive row outside the buffer's rows
  *  - bf16 tensors are raw 16-bit bfloat16 patterns, row-major.
  *  - T*k rows always suffice for a receive buffer (top-k picks k distinct
  *    experts per token), so buffers are sized without reading any count
- *    back to the host.
+ *    back to the host.  Calls that read or write a receive buffer take its
+ *    row count (recv_rows / y_rows): T*k after ep_get_layout, E*capacity
+ *    after ep_get_layout_capacity.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
@@ -68,8 +70,9 @@ typedef enum {
 } ep_score_fn;
 
 typedef enum {
-    EP_DTYPE_BF16 = 0,         /* receive rows are bf16 copies of x */
-    EP_DTYPE_FP8_E4M3_B128 = 1 /* receive rows are e4m3 codes + one fp32 scale per 128 columns */
+    EP_DTYPE_BF16 = 0,          /* receive rows are bf16 copies of x */
+    EP_DTYPE_FP8_E4M3_B128 = 1, /* e4m3 codes + one fp32 scale per 128 columns */
+    EP_DTYPE_MXFP8_E4M3_B32 = 2 /* MXFP8: e4m3 codes + one E8M0 (power-of-two) scale byte per 32 columns */
 } ep_dtype;
 
 /* Gating configuration (see ep_gate). */
@@ -173,46 +176,121 @@ ep_status ep_get_layout_noalloc(const int32_t *topk_idx, int32_t T, int32_t k, i
 
 /*
  * Step 3 -- permute-scatter ("Expert Parallelism ...", section "Le pattern
- * de communication all-to-all", Phase 1; FP8 mode from "DeepEP de DeepSeek
+ * de communication all-to-all", Phase 1; FP8 modes from "DeepEP de DeepSeek
  * ...", section "Support FP8 et MXFP8").
  *
  * x            [T, H] bf16, 16-byte aligned; H % 8 == 0.
  * pos          [T, k] int32 receive row per entry (from ep_get_layout);
- *              entries < 0 are skipped; rows >= T*k are skipped and flagged
- *              EP_FLAG_BAD_ROW.
- * dtype        EP_DTYPE_BF16: recv [T*k, H] bf16, recv[pos[t,j]] = x[t].
+ *              entries < 0 are skipped; rows >= recv_rows are skipped and
+ *              flagged EP_FLAG_BAD_ROW.  1 <= k <= 64.
+ * recv_rows    rows of recv (and of recv_scales), >= 0.
+ * dtype        EP_DTYPE_BF16: recv [T*k, H] bf16, recv[pos[t,j]] = x[t];
+ *              recv_scales unused (may be NULL).
  *              EP_DTYPE_FP8_E4M3_B128 (needs H % 128 == 0): recv [T*k, H]
- *              e4m3 bytes and recv_scales [T*k, H/128] fp32; per token and
+ *              e4m3 bytes and recv_scales fp32 [T*k, H/128]; per token and
  *              128-column block b: s = amax|x[t, b]| / 448 (fp32 IEEE
  *              division), code = e4m3(x / s) with an fp32 IEEE division and
  *              round-to-nearest-even saturating to +-448; a block with
- *              amax = 0 gets s = 0 and signed-zero codes.  Every copy of a
- *              token carries the same codes and scales.
- * recv         16-byte aligned.  recv_scales: 4-byte aligned, NULL for BF16.
+ *              amax = 0 gets s = 0 and signed-zero codes.
+ *              EP_DTYPE_MXFP8_E4M3_B32 (needs H % 32 == 0; the OCP
+ *              Microscaling MXFP8 format): recv [T*k, H] e4m3 bytes and
+ *              recv_scales uint8 [T*k, H/32] E8M0 bytes; per 32-column block
+ *              e = floor(log2 amax) - 8 clamped to [-127, 127] (amax = 0:
+ *              -127), byte = e + 127, code = e4m3(x * 2^-e) nearest-even,
+ *              saturating.
+ *              Every copy of a token carries the same codes and scales.
+ * recv         16-byte aligned.  recv_scales: 4-byte aligned for fp32.
  * Rows of recv not named by pos are left untouched.
- * Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED (FP8 with H % 128 != 0),
- * EP_ERR_ALIGNMENT, EP_ERR_CUDA.
+ * Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED (H % 8, H % 128 for FP8,
+ * H % 32 for MXFP8, k > 64), EP_ERR_ALIGNMENT, EP_ERR_CUDA.
  */
 ep_status ep_dispatch(const void *x, int32_t T, int32_t H, int32_t k, const int32_t *pos,
-                      int32_t dtype, void *recv, float *recv_scales, int32_t *err_flag,
-                      void *stream);
+                      int32_t dtype, void *recv, int32_t recv_rows, void *recv_scales,
+                      int32_t *err_flag, void *stream);
 
 /*
  * Steps 4 and 5 -- inverse gather and weighted combine ("Expert Parallelism
  * ...", section "Le pattern de communication all-to-all", Phase 2: results
  * return to their token and are combined weighted by the router scores).
  *
- * y       [T*k, H] bf16 expert outputs in receive-row order, 16-byte aligned.
+ * y       [y_rows, H] bf16 expert outputs in receive-row order, 16-byte
+ *         aligned (y_rows = T*k after ep_get_layout).
  * pos     [T, k] int32 (from ep_get_layout); entries < 0 contribute nothing,
- *         rows >= T*k contribute nothing and are flagged EP_FLAG_BAD_ROW.
+ *         rows >= y_rows contribute nothing and are flagged EP_FLAG_BAD_ROW.
  * topk_w  [T, k] fp32 router weights.
  * out     [T, H] bf16, 16-byte aligned:
  *         out[t, h] = bf16_rne( fma chain over j = 0..k-1 in slot order of
  *         w[t, j] * y[pos[t, j], h], accumulated in fp32 from 0 ).
  * H % 8 == 0.  Errors: EP_ERR_INVALID_ARG, EP_ERR_ALIGNMENT, EP_ERR_CUDA.
  */
-ep_status ep_combine(const void *y, const int32_t *pos, const float *topk_w, int32_t T, int32_t H,
-                     int32_t k, void *out, int32_t *err_flag, void *stream);
+ep_status ep_combine(const void *y, int32_t y_rows, const int32_t *pos, const float *topk_w, int32_t T,
+                     int32_t H, int32_t k, void *out, int32_t *err_flag, void *stream);
+
+/*
+ * Steps 4 and 5 on FP8 expert outputs ("DeepEP de DeepSeek ...", section
+ * "Support FP8 et MXFP8": FP8 payloads in both directions halve the bytes).
+ *
+ * yq           [y_rows, H] e4m3 codes, 16-byte aligned.
+ * yscales      scale_dtype EP_DTYPE_FP8_E4M3_B128: fp32 [y_rows, H/128];
+ *              EP_DTYPE_MXFP8_E4M3_B32: E8M0 bytes [y_rows, H/32].
+ * pos, topk_w, out, err_flag as in ep_combine.
+ * out[t, h] = bf16_rne( fp32 fma chain over j of w[t,j] * (e4m3 value of
+ * yq[pos[t,j], h] * its block scale) ), the dequantised product taken in
+ * fp32.  Errors as ep_combine, plus EP_ERR_UNSUPPORTED when H is not a
+ * multiple of the block width.
+ */
+ep_status ep_combine_fp8(const void *yq, const void *yscales, int32_t scale_dtype, int32_t y_rows,
+                         const int32_t *pos, const float *topk_w, int32_t T, int32_t H, int32_t k,
+                         void *out, int32_t *err_flag, void *stream);
+
+/*
+ * Capacity-limited layout: the capacity factor / token dropping lever of
+ * "Expert Parallelism ...", section "Defis et optimisations" (Load
+ * balancing).  Expert e owns the fixed receive rows [e*capacity,
+ * (e+1)*capacity); entries are taken in flat (token, slot) order and an
+ * expert's entries past its first `capacity` are dropped (pos = -1; a
+ * combine then gives them no weight).  capacity >= 0; a capacity factor f
+ * gives capacity = ceil(f * T * k / E).
+ *
+ * Outputs as ep_get_layout, except: expert_count[E] = kept entries;
+ * expert_off[e] = e*capacity; rank_count[R] = kept entries of the rank;
+ * rank_off[r] = r*experts_per_rank*capacity; rank_tokens[R] = distinct
+ * tokens with a kept entry on the rank; expert_dropped[E] = entries past
+ * capacity; src has E*capacity rows (-1 for an empty row).  The receive
+ * buffer needs E*capacity rows.  workspace as ep_get_layout.  Limits as
+ * ep_get_layout and E*capacity < 2^31.
+ */
+ep_status ep_get_layout_capacity(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E,
+                                 int32_t experts_per_rank, int32_t capacity, int32_t *expert_count,
+                                 int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                                 int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos,
+                                 int32_t *src, int32_t *err_flag, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of the BF16 dispatch (a k-fold copy): the gradient of a source
+ * row is the sum of its copies' gradients,
+ *   grad_x[t, h] = bf16_rne( fp32 sum over j in slot order of grad_recv[pos[t,j], h] ),
+ * a token with no copy getting zeros.  grad_recv [recv_rows, H] bf16, grad_x
+ * [T, H] bf16, both 16-byte aligned; pos, k, H, err_flag as in ep_combine.
+ * (Training is the pages' main setting: "DeepEP de DeepSeek ...", forward
+ * and backward passes of pretraining.)
+ */
+ep_status ep_dispatch_backward(const void *grad_recv, int32_t recv_rows, const int32_t *pos, int32_t T,
+                               int32_t H, int32_t k, void *grad_x, int32_t *err_flag, void *stream);
+
+/*
+ * Backward of the weighted combine out[t] = sum_j w[t,j] * y[pos[t,j]]:
+ *   grad_y[pos[t,j], h] = bf16_rne(w[t,j] * grad_out[t, h])  (the exact product
+ *                         rounded once, for products in fp32's normal range)
+ *   grad_w[t, j]        = sum_h grad_out[t, h] * y[pos[t,j], h]  (fp32, fixed
+ *                         reduction order; 0 for an empty slot)
+ * grad_out [T, H] bf16, y and grad_y [y_rows, H] bf16 (16-byte aligned; rows
+ * of grad_y not named by pos untouched), topk_w and grad_w [T, k] fp32.
+ */
+ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_rows, const int32_t *pos,
+                              const float *topk_w, int32_t T, int32_t H, int32_t k, void *grad_y,
+                              float *grad_w, int32_t *err_flag, void *stream);
 
 /* Static description of a status code. */
 const char *ep_status_str(ep_status s);

@@ -50,6 +50,14 @@ def _load():
         lib.orc_e4m3_decode_array.restype = None
         lib.orc_bf16_from_double_array.argtypes = [P, P, i64]
         lib.orc_bf16_from_double_array.restype = None
+        lib.orc_dispatch_mxfp8.argtypes = [P, i32, i32, i32, P, P, P]
+        lib.orc_combine_fp8.argtypes = [P, P, i32, P, P, i32, i32, i32, P]
+        lib.orc_layout_capacity.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.orc_dispatch_backward.argtypes = [P, P, i32, i32, i32, P]
+        lib.orc_combine_backward.argtypes = [P, P, P, P, i32, i32, i32, P, P]
+        for f in ("orc_dispatch_mxfp8", "orc_combine_fp8", "orc_layout_capacity", "orc_dispatch_backward",
+                  "orc_combine_backward"):
+            getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -164,3 +172,89 @@ def bf16_from_double(v):
     out = np.empty(a.shape, np.uint16)
     _load().orc_bf16_from_double_array(_ptr(a), _ptr(out), a.size)
     return out
+
+
+def dispatch_mxfp8(x_bits, pos, recv_q=None, recv_e=None):
+    """MXFP8 (E4M3 elements, E8M0 scale per 32 columns) dispatch.
+    Returns (codes uint8 [T*k,H], scale exponents uint8 [T*k,H/32])."""
+    x = _c(x_bits, np.uint16)
+    p = _c(pos, np.int32)
+    T, H = x.shape
+    k = p.shape[1]
+    if H % 32:
+        raise ValueError("oracle dispatch_mxfp8: H must be a multiple of 32")
+    if recv_q is None:
+        recv_q = np.zeros((T * k, H), np.uint8)
+    if recv_e is None:
+        recv_e = np.zeros((T * k, H // 32), np.uint8)
+    if _load().orc_dispatch_mxfp8(_ptr(x), T, H, k, _ptr(p), _ptr(recv_q), _ptr(recv_e)) != 0:
+        raise ValueError("oracle dispatch_mxfp8: invalid arguments")
+    return recv_q, recv_e
+
+
+def combine_fp8(yq, yscale, pos, w):
+    """Combine of FP8 expert outputs.  yscale float32 [rows, H/128] (1x128
+    fp32 scales) or uint8 [rows, H/32] (E8M0).  Returns uint16 bf16 [T,H]."""
+    q = _c(yq, np.uint8)
+    p = _c(pos, np.int32)
+    wf = _c(w, np.float32)
+    kind = 0 if np.asarray(yscale).dtype == np.float32 else 1
+    sc = _c(yscale, np.float32 if kind == 0 else np.uint8)
+    T, k = p.shape
+    H = q.shape[1]
+    out = np.empty((T, H), np.uint16)
+    if _load().orc_combine_fp8(_ptr(q), _ptr(sc), kind, _ptr(p), _ptr(wf), T, H, k, _ptr(out)) != 0:
+        raise ValueError("oracle combine_fp8: invalid arguments")
+    return out
+
+
+def layout_capacity(topk_idx, num_experts, experts_per_rank, capacity):
+    """Capacity-limited layout (fixed rows [e*capacity, (e+1)*capacity))."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    E = num_experts
+    if experts_per_rank <= 0 or E % experts_per_rank or capacity < 0:
+        raise ValueError("oracle layout_capacity: invalid arguments")
+    R = E // experts_per_rank
+    out = dict(
+        expert_count=np.empty(E, np.int32), expert_off=np.empty(E + 1, np.int32),
+        rank_count=np.empty(R, np.int32), rank_off=np.empty(R + 1, np.int32),
+        rank_tokens=np.empty(R, np.int32), expert_dropped=np.empty(E, np.int32),
+        pos=np.empty((T, k), np.int32), src=np.empty(E * capacity, np.int32))
+    err = np.zeros(1, np.int32)
+    rc = _load().orc_layout_capacity(_ptr(idx), T, k, E, experts_per_rank, capacity, _ptr(out["expert_count"]),
+                                     _ptr(out["expert_off"]), _ptr(out["rank_count"]), _ptr(out["rank_off"]),
+                                     _ptr(out["rank_tokens"]), _ptr(out["expert_dropped"]), _ptr(out["pos"]),
+                                     _ptr(out["src"]), _ptr(err))
+    if rc != 0:
+        raise ValueError("oracle layout_capacity: invalid arguments")
+    out["err_flag"] = int(err[0])
+    return out
+
+
+def dispatch_backward(grad_recv_bits, pos):
+    """grad_x[t] = bf16(sum_j grad_recv[pos[t,j]]).  Returns uint16 [T,H]."""
+    g = _c(grad_recv_bits, np.uint16)
+    p = _c(pos, np.int32)
+    T, k = p.shape
+    H = g.shape[1]
+    out = np.empty((T, H), np.uint16)
+    if _load().orc_dispatch_backward(_ptr(g), _ptr(p), T, H, k, _ptr(out)) != 0:
+        raise ValueError("oracle dispatch_backward: invalid arguments")
+    return out
+
+
+def combine_backward(grad_out_bits, y_bits, pos, w, grad_y=None):
+    """Returns (grad_y uint16 [T*k,H], grad_w float64 [T,k])."""
+    go = _c(grad_out_bits, np.uint16)
+    y = _c(y_bits, np.uint16)
+    p = _c(pos, np.int32)
+    wf = _c(w, np.float32)
+    T, k = p.shape
+    H = go.shape[1]
+    if grad_y is None:
+        grad_y = np.zeros((y.shape[0], H), np.uint16)
+    gw = np.empty((T, k), np.float64)
+    if _load().orc_combine_backward(_ptr(go), _ptr(y), _ptr(p), _ptr(wf), T, H, k, _ptr(grad_y), _ptr(gw)) != 0:
+        raise ValueError("oracle combine_backward: invalid arguments")
+    return grad_y, gw

@@ -448,3 +448,212 @@ int orc_combine(const uint16_t *y, const int32_t *pos, const float *w, int32_t T
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Next rows: MXFP8, FP8-input combine, capacity, backward                   */
+/* ------------------------------------------------------------------------ */
+
+/* MXFP8 (OCP Microscaling Formats v1.0, MXFP8 with E4M3 elements): blocks of
+ * 32 columns share one power-of-two scale X = 2^e with
+ * e = floor(log2(amax)) - 8 (8 = exponent of E4M3's largest normal, 448 =
+ * 1.75 * 2^8), clamped to [-127, 127] and stored as the E8M0 byte e + 127.
+ * Elements are e4m3(x / X), nearest-even, saturating; x / X is exact (a
+ * power-of-two scaling).  A block with amax = 0 gets e = -127 (byte 0) and
+ * signed-zero codes.  The pages name MXFP8 ("DeepEP de DeepSeek ...",
+ * section "Support FP8 et MXFP8") without defining it; the definition is the
+ * OCP one.  recv_q [T*k, H] bytes, recv_e [T*k, H/32] E8M0 bytes.
+ * H % 32 == 0. */
+int orc_dispatch_mxfp8(const uint16_t *x, int32_t T, int32_t H, int32_t k, const int32_t *pos,
+                       uint8_t *recv_q, uint8_t *recv_e)
+{
+    if (T < 0 || H <= 0 || H % 32 != 0 || k <= 0)
+        return -1;
+    const int32_t nb = H / 32;
+    uint8_t *q = malloc((size_t)H);
+    uint8_t *eb = malloc((size_t)nb);
+    if (!q || !eb) {
+        free(q); free(eb);
+        return -1;
+    }
+    for (int32_t t = 0; t < T; ++t) {
+        const uint16_t *row = x + (int64_t)t * H;
+        for (int32_t b = 0; b < nb; ++b) {
+            double amax = 0.0;
+            for (int32_t c = 0; c < 32; ++c) {
+                double a = fabs((double)bf16_bits_to_float(row[b * 32 + c]));
+                if (a > amax)
+                    amax = a;
+            }
+            int e = (amax == 0.0) ? -127 : ilogb(amax) - 8;
+            if (e < -127)
+                e = -127;
+            if (e > 127)
+                e = 127;
+            eb[b] = (uint8_t)(e + 127);
+            for (int32_t c = 0; c < 32; ++c) {
+                double v = (double)bf16_bits_to_float(row[b * 32 + c]);
+                double scaled = ldexp(v, -e);               /* exact */
+                if (amax == 0.0)
+                    q[b * 32 + c] = signbit(v) ? 0x80u : 0x00u;
+                else  /* (float) is exact, or flushes a far-below-2^-10 value to a signed zero */
+                    q[b * 32 + c] = orc_e4m3_encode((float)scaled);
+            }
+        }
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t p = pos[(int64_t)t * k + j];
+            if (p < 0)
+                continue;
+            memcpy(recv_q + (int64_t)p * H, q, (size_t)H);
+            memcpy(recv_e + (int64_t)p * nb, eb, (size_t)nb);
+        }
+    }
+    free(q);
+    free(eb);
+    return 0;
+}
+
+/* Combine of FP8 expert outputs: the dequantised value of a code is its E4M3
+ * value times its block's scale -- fp32 scales per 128 columns
+ * (scale_kind 0) or E8M0 powers of two per 32 columns (scale_kind 1).
+ * out[t, h] = bf16( sum_j w[t, j] * dequant(yq[pos[t, j], h]) ) in binary64. */
+int orc_combine_fp8(const uint8_t *yq, const void *yscale, int32_t scale_kind, const int32_t *pos, const float *w,
+                    int32_t T, int32_t H, int32_t k, uint16_t *out)
+{
+    if (T < 0 || H <= 0 || k <= 0 || (scale_kind != 0 && scale_kind != 1))
+        return -1;
+    const int32_t bs = scale_kind == 0 ? 128 : 32;
+    if (H % bs != 0)
+        return -1;
+    const int32_t nb = H / bs;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t p = pos[(int64_t)t * k + j];
+                if (p < 0)
+                    continue;
+                double s = scale_kind == 0 ? (double)((const float *)yscale)[(int64_t)p * nb + h / bs]
+                                           : ldexp(1.0, (int)((const uint8_t *)yscale)[(int64_t)p * nb + h / bs] - 127);
+                acc += (double)w[(int64_t)t * k + j] * (orc_e4m3_decode(yq[(int64_t)p * H + h]) * s);
+            }
+            out[(int64_t)t * H + h] = orc_bf16_from_double(acc);
+        }
+    return 0;
+}
+
+/* Capacity-limited layout: expert e owns the fixed receive rows
+ * [e * capacity, (e + 1) * capacity).  Entries are taken in flat (token,
+ * slot) order; an expert's first `capacity` entries get its rows in that
+ * order, later ones are dropped (pos = -1) -- the capacity factor / token
+ * dropping lever of "Expert Parallelism (Parallelisme d'experts)", section
+ * "Defis et optimisations" (Load balancing).  Outputs as orc_layout, with:
+ * expert_count[E] = kept entries, expert_off[e] = e * capacity,
+ * rank_count[R] = kept entries of the rank, rank_off[r] = r * epr * capacity,
+ * rank_tokens[R] = distinct tokens with a kept entry on the rank,
+ * expert_dropped[E] = entries past capacity, src[E * capacity] = flat entry
+ * of each row or -1 for an empty row. */
+int orc_layout_capacity(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E, int32_t experts_per_rank,
+                        int32_t capacity, int32_t *expert_count, int32_t *expert_off, int32_t *rank_count,
+                        int32_t *rank_off, int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos,
+                        int32_t *src, int32_t *err_flag)
+{
+    if (T < 0 || k <= 0 || E <= 0 || experts_per_rank <= 0 || E % experts_per_rank != 0 || capacity < 0)
+        return -1;
+    const int32_t R = E / experts_per_rank;
+    const int64_t N = (int64_t)T * k;
+    int32_t err = 0;
+    memset(expert_count, 0, sizeof(int32_t) * (size_t)E);
+    memset(expert_dropped, 0, sizeof(int32_t) * (size_t)E);
+    for (int64_t i = 0; i < (int64_t)E * capacity; ++i)
+        src[i] = -1;
+    for (int64_t i = 0; i < N; ++i) {
+        int32_t e = topk_idx[i];
+        pos[i] = -1;
+        if (e < 0 || e >= E) {
+            if (e != -1)
+                err |= 1;
+            continue;
+        }
+        if (expert_count[e] < capacity) {
+            pos[i] = e * capacity + expert_count[e];
+            src[pos[i]] = (int32_t)i;
+            expert_count[e] += 1;
+        } else {
+            expert_dropped[e] += 1;
+        }
+    }
+    for (int32_t e = 0; e <= E; ++e)
+        expert_off[e] = e * capacity;
+    for (int32_t r = 0; r <= R; ++r)
+        rank_off[r] = r * experts_per_rank * capacity;
+    char *touched = malloc((size_t)R);
+    if (!touched)
+        return -1;
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t c = 0;
+        for (int32_t e = r * experts_per_rank; e < (r + 1) * experts_per_rank; ++e)
+            c += expert_count[e];
+        rank_count[r] = c;
+        rank_tokens[r] = 0;
+    }
+    for (int32_t t = 0; t < T; ++t) {
+        memset(touched, 0, (size_t)R);
+        for (int32_t j = 0; j < k; ++j)
+            if (pos[(int64_t)t * k + j] >= 0)
+                touched[topk_idx[(int64_t)t * k + j] / experts_per_rank] = 1;
+        for (int32_t r = 0; r < R; ++r)
+            rank_tokens[r] += touched[r];
+    }
+    free(touched);
+    if (err_flag)
+        *err_flag |= err;
+    return 0;
+}
+
+/* Backward of the BF16 dispatch (a copy): each source row's gradient is the
+ * sum of its copies' gradients, grad_x[t] = bf16( sum_j grad_recv[pos[t,j]] )
+ * in binary64; a token with no copy gets zeros. */
+int orc_dispatch_backward(const uint16_t *grad_recv, const int32_t *pos, int32_t T, int32_t H, int32_t k,
+                          uint16_t *grad_x)
+{
+    if (T < 0 || H <= 0 || k <= 0)
+        return -1;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t p = pos[(int64_t)t * k + j];
+                if (p >= 0)
+                    acc += (double)bf16_bits_to_float(grad_recv[(int64_t)p * H + h]);
+            }
+            grad_x[(int64_t)t * H + h] = orc_bf16_from_double(acc);
+        }
+    return 0;
+}
+
+/* Backward of the weighted combine out[t] = sum_j w[t,j] * y[pos[t,j]]:
+ * grad_y[pos[t,j], h] = bf16( w[t,j] * grad_out[t,h] ) (exact product, one
+ * rounding) and grad_w[t,j] = sum_h grad_out[t,h] * y[pos[t,j], h]
+ * (binary64; 0 for an empty slot).  Rows of grad_y no entry names are left
+ * untouched. */
+int orc_combine_backward(const uint16_t *grad_out, const uint16_t *y, const int32_t *pos, const float *w,
+                         int32_t T, int32_t H, int32_t k, uint16_t *grad_y, double *grad_w)
+{
+    if (T < 0 || H <= 0 || k <= 0)
+        return -1;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t p = pos[(int64_t)t * k + j];
+            double dot = 0.0;
+            if (p >= 0) {
+                double wj = (double)w[(int64_t)t * k + j];
+                for (int32_t h = 0; h < H; ++h) {
+                    double g = (double)bf16_bits_to_float(grad_out[(int64_t)t * H + h]);
+                    grad_y[(int64_t)p * H + h] = orc_bf16_from_double(wj * g);
+                    dot += g * (double)bf16_bits_to_float(y[(int64_t)p * H + h]);
+                }
+            }
+            grad_w[(int64_t)t * k + j] = dot;
+        }
+    return 0;
+}

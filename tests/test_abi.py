@@ -95,24 +95,29 @@ def test_layout_host_checks(lib):
 
 def test_dispatch_host_checks(lib):
     d = lib.ep_dispatch
-    assert d(FAKE, 16, 7168, 8, FAKE, 2, FAKE, FAKE, None, None) == 1          # unknown dtype
-    assert d(FAKE, 16, 7164, 8, FAKE, 0, FAKE, None, None, None) == 2          # H % 8
-    assert d(FAKE, 16, 7232, 8, FAKE, 1, FAKE, FAKE, None, None) == 2          # FP8 needs H % 128
-    assert d(FAKE, 16, 7168, 65, FAKE, 0, FAKE, None, None, None) == 2         # k > 64
-    assert d(FAKE, 16, 7168, 8, FAKE, 1, FAKE, None, None, None) == 1          # FP8 without scales
-    assert d(ctypes.c_void_p(0x10008), 16, 7168, 8, FAKE, 0, FAKE, None, None, None) == 3
-    assert d(FAKE, 16, 7168, 8, FAKE, 0, ODD, None, None, None) == 3
-    assert d(None, 0, 7168, 8, None, 0, None, None, None, None) == 0           # empty batch
-    assert d(FAKE, 16, 0, 8, FAKE, 0, FAKE, None, None, None) == 1
+    R = 128
+    assert d(FAKE, 16, 7168, 8, FAKE, 3, FAKE, R, FAKE, None, None) == 1          # unknown dtype
+    assert d(FAKE, 16, 7184, 8, FAKE, 2, FAKE, R, FAKE, None, None) == 2          # MXFP8 needs H % 32
+    assert d(FAKE, 16, 7168, 8, FAKE, 2, FAKE, R, None, None, None) == 1          # MXFP8 without scales
+    assert d(FAKE, 16, 7164, 8, FAKE, 0, FAKE, R, None, None, None) == 2          # H % 8
+    assert d(FAKE, 16, 7232, 8, FAKE, 1, FAKE, R, FAKE, None, None) == 2          # FP8 needs H % 128
+    assert d(FAKE, 16, 7168, 65, FAKE, 0, FAKE, R, None, None, None) == 2         # k > 64
+    assert d(FAKE, 16, 7168, 8, FAKE, 1, FAKE, R, None, None, None) == 1          # FP8 without scales
+    assert d(FAKE, 16, 7168, 8, FAKE, 0, FAKE, -1, None, None, None) == 1         # negative row count
+    assert d(ctypes.c_void_p(0x10008), 16, 7168, 8, FAKE, 0, FAKE, R, None, None, None) == 3
+    assert d(FAKE, 16, 7168, 8, FAKE, 0, ODD, R, None, None, None) == 3
+    assert d(None, 0, 7168, 8, None, 0, None, 0, None, None, None) == 0           # empty batch
+    assert d(FAKE, 16, 0, 8, FAKE, 0, FAKE, R, None, None, None) == 1
 
 
 def test_combine_host_checks(lib):
     c = lib.ep_combine
-    assert c(FAKE, FAKE, FAKE, 16, 7164, 8, FAKE, None, None) == 2
-    assert c(FAKE, FAKE, FAKE, 16, 7168, 0, FAKE, None, None) == 1
-    assert c(None, FAKE, FAKE, 16, 7168, 8, FAKE, None, None) == 1
-    assert c(FAKE, FAKE, FAKE, 16, 7168, 8, ODD, None, None) == 3
-    assert c(None, None, None, 0, 7168, 8, None, None, None) == 0
+    assert c(FAKE, 128, FAKE, FAKE, 16, 7164, 8, FAKE, None, None) == 2
+    assert c(FAKE, 128, FAKE, FAKE, 16, 7168, 0, FAKE, None, None) == 1
+    assert c(None, 128, FAKE, FAKE, 16, 7168, 8, FAKE, None, None) == 1
+    assert c(FAKE, -3, FAKE, FAKE, 16, 7168, 8, FAKE, None, None) == 1
+    assert c(FAKE, 128, FAKE, FAKE, 16, 7168, 8, ODD, None, None) == 3
+    assert c(None, 0, None, None, 0, 7168, 8, None, None, None) == 0
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch):
@@ -121,3 +126,28 @@ def test_binding_fails_loudly_without_the_library(monkeypatch):
     monkeypatch.setattr(_binding, "LIB_PATH", os.path.join(ROOT, "no_such_lib.so"))
     with pytest.raises(ImportError):
         _binding.load()
+
+
+def test_next_row_entry_points_host_checks(lib):
+    cf = lib.ep_combine_fp8
+    assert cf(FAKE, FAKE, 0, 128, FAKE, FAKE, 16, 7168, 8, FAKE, None, None) == 1   # bf16 is no FP8 scale kind
+    assert cf(FAKE, FAKE, 1, 128, FAKE, FAKE, 16, 7232, 8, FAKE, None, None) == 2   # 1x128 needs H % 128
+    assert cf(FAKE, FAKE, 2, 128, FAKE, FAKE, 16, 7184, 8, FAKE, None, None) == 2   # MXFP8 needs H % 32
+    assert cf(FAKE, None, 2, 128, FAKE, FAKE, 16, 7168, 8, FAKE, None, None) == 1
+    assert cf(FAKE, FAKE, 2, 128, FAKE, FAKE, 16, 7168, 8, ODD, None, None) == 3
+    assert cf(None, None, 2, 0, None, None, 0, 7168, 8, None, None, None) == 0
+    n = lib.ep_layout_workspace_bytes(64, 8, 256, 8)
+    lc = lambda T, cap, ws=FAKE, E=256: lib.ep_get_layout_capacity(  # noqa: E731
+        FAKE, T, 8, E, 8, cap, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, ws, n, None)
+    assert lc(64, -1) == 1
+    assert lc(64, 1 << 24) == 2                                                     # E * capacity overflows
+    assert lc(64, 16, ws=None) == 1
+    assert lc(64, 16, E=2048) == 2
+    db = lib.ep_dispatch_backward
+    assert db(FAKE, 128, FAKE, 16, 7164, 8, FAKE, None, None) == 2
+    assert db(FAKE, 128, FAKE, 16, 7168, 8, ODD, None, None) == 3
+    assert db(None, 0, None, 0, 7168, 8, None, None, None) == 0
+    cb = lib.ep_combine_backward
+    assert cb(FAKE, FAKE, 128, FAKE, FAKE, 16, 7168, 0, FAKE, FAKE, None, None) == 1
+    assert cb(FAKE, FAKE, 128, FAKE, FAKE, 16, 7168, 8, ODD, FAKE, None, None) == 3
+    assert cb(FAKE, None, 128, FAKE, FAKE, 16, 7168, 8, FAKE, FAKE, None, None) == 1
