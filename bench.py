@@ -443,16 +443,122 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def op_bytes(cfg):
+    """Algorithmic bytes of every op over the whole batch (bench sweep)."""
+    T, H, E, k = cfg["T"], cfg["H"], cfg["E"], cfg["k"]
+    fp8_row = H + H // 32                          # e4m3 codes + scales (1x128 fp32 or 1x32 E8M0)
+    b = algorithmic_bytes(cfg)
+    return {
+        "gate": b["gate"], "layout": b["layout"], "layout_capacity": b["layout"],
+        "dispatch_bf16": b["dispatch_bf16"], "dispatch_fp8": b["dispatch_fp8"],
+        "dispatch_mxfp8": T * (2 * H + k * fp8_row + 4 * k),
+        "combine": b["combine"], "combine_fp8": T * (k * fp8_row + 8 * k + 2 * H),
+        "combine_mxfp8": T * (k * fp8_row + 8 * k + 2 * H),
+        "dispatch_backward": T * (2 * H * k + 4 * k + 2 * H),
+        "combine_backward": T * (2 * H + 4 * H * k + 12 * k),
+        "decode_fused": b["gate"] + b["layout"] + b["dispatch_fp8"],
+    }
+
+
+def run_sweep(args):
+    """--sweep: every op on every workload, one JSON line per workload."""
+    import torch
+
+    import combine_group_limited_gb300 as ep
+    from combine_group_limited_gb300 import build as epbuild
+    epbuild.build()
+    torch.cuda.set_device(0)
+    peak, peak_kind = measured_hbm_peak()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda").fill_(1)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        ts = []
+        for i in range(reps + 3):
+            flush.fill_(i & 0xFF)
+            flush_rd.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    names = args.configs.split(",") if args.configs else list(synth.CONFIGS)
+    for name in names:
+        cfg = synth.config(name)
+        T, H, E, k, epr = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["experts_per_rank"]
+        r = PathRunner(cfg)
+        gc = r.gcfg
+        cap = -(-T * k // E)
+        recv_b = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda")
+        recv_mq = torch.empty((T * k, H), dtype=torch.uint8, device="cuda")
+        recv_me = torch.empty((T * k, H // 32), dtype=torch.uint8, device="cuda")
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        gy = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda")
+        gw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        ws = r.ws
+        ops = {
+            "gate": lambda: r.gate(),
+            "layout": lambda: r.layout(),
+            "layout_capacity": lambda: ep.ep_get_layout_capacity(r.topk_idx, E, epr, cap, workspace=ws),
+            "dispatch_bf16": lambda: ep.ep_dispatch(r.x, r.lay.pos, "bf16", recv=recv_b),
+            "dispatch_mxfp8": lambda: ep.ep_dispatch(r.x, r.lay.pos, "mxfp8", recv=recv_mq, recv_scales=recv_me),
+            "combine": lambda: r.combine(),
+            "combine_mxfp8": lambda: ep.ep_combine_fp8(recv_mq, recv_me, r.lay.pos, r.topk_w, out=out),
+            "dispatch_backward": lambda: ep.ep_dispatch_backward(r.y, r.lay.pos, out=out),
+            "combine_backward": lambda: ep.ep_combine_backward(r.x, r.y, r.lay.pos, r.topk_w, grad_y=gy, grad_w=gw),
+        }
+        if H % 128 == 0:
+            ops["dispatch_fp8"] = lambda: r.dispatch()
+            ops["combine_fp8"] = lambda: ep.ep_combine_fp8(r.recv_q, r.recv_s, r.lay.pos, r.topk_w, out=out)
+        if T * k <= 4096 and H % 128 == 0:
+            dws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+            ops["decode_fused"] = lambda: ep.ep_decode_dispatch(
+                r.scores, r.bias, gc, epr, r.x, "fp8", topk_idx=r.topk_idx, topk_w=r.topk_w, out=r.lay,
+                recv=r.recv_q, recv_scales=r.recv_s, workspace=dws)
+        # run every op once so that its inputs exist (mxfp8 codes for its combine)
+        for fn in ops.values():
+            fn()
+        torch.cuda.synchronize()
+        nb = op_bytes(cfg)
+        res = {}
+        for op, fn in ops.items():
+            us = timed(fn, args.reps)
+            gbs = nb[op] / (us * 1e-6) / 1e9
+            res[op] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb[op]}
+        dsp = "dispatch_fp8" if H % 128 == 0 else "dispatch_bf16"
+        step = lambda: (r.gate(), r.layout(), ops[dsp](), r.combine())  # noqa: E731
+        step_us = timed(step, args.reps)
+        if "decode_fused" in ops:
+            sep = lambda: (r.gate(), r.layout(), r.dispatch())  # noqa: E731
+            res["decode_separate"] = {"us": round(timed(sep, args.reps), 2)}
+        line = {"sweep": name, "T": T, "H": H, "E": E, "k": k, "peak_GBs": peak, "peak_source": peak_kind,
+                "step_us": round(step_us, 2), "step_tokens_per_s": round(T / (step_us * 1e-6), 1),
+                "step_dispatch": dsp, "ops": res}
+        print(json.dumps(line), flush=True)
+        del r, recv_b, recv_mq, recv_me, out, gy, gw, ops
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep", action="store_true", help="time every op on every workload (one line each)")
+    ap.add_argument("--configs", default="", help="comma-separated workloads for --sweep")
+    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per op in --sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -16,14 +16,14 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libep_gb300.so")
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_ALIGNMENT, EP_ERR_CUDA = range(5)
-EP_FLAG_BAD_EXPERT, EP_FLAG_BAD_ROW = 1, 2
+EP_FLAG_BAD_EXPERT, EP_FLAG_BAD_ROW, EP_FLAG_TIMEOUT = 1, 2, 4
 EP_SCORE_RAW, EP_SCORE_SOFTMAX = 0, 1
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128, EP_DTYPE_MXFP8_E4M3_B32 = 0, 1, 2
 
 # Symbols include/ep.h declares (checked by the CPU test suite).
 EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch",
            "ep_combine", "ep_combine_fp8", "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward",
-           "ep_status_str")
+           "ep_decode_dispatch", "ep_selftest_grid_barrier", "ep_status_str")
 
 
 class GateCfg(ctypes.Structure):
@@ -62,8 +62,12 @@ def load():
     lib.ep_get_layout_capacity.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
     lib.ep_dispatch_backward.argtypes = [P, i32, P, i32, i32, i32, P, P, P]
     lib.ep_combine_backward.argtypes = [P, P, i32, P, P, i32, i32, i32, P, P, P, P]
+    lib.ep_decode_dispatch.argtypes = [P, P, i32, ctypes.POINTER(GateCfg), i32, P, i32, i32, P, P, P, P, P, P, P, P,
+                                       P, P, i32, P, P, P, sz, P]
+    lib.ep_selftest_grid_barrier.argtypes = [i32, ctypes.c_int64, P, P, sz, P]
     for f in ("ep_gate", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_combine", "ep_combine_fp8",
-              "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward"):
+              "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward", "ep_decode_dispatch",
+              "ep_selftest_grid_barrier"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ep_status_str.argtypes = [ctypes.c_int]
     lib.ep_status_str.restype = ctypes.c_char_p
@@ -343,3 +347,53 @@ def ep_combine_backward(grad_out, y, pos, topk_w, grad_y=None, grad_w=None, err_
         _ptr(grad_out), _ptr(y), y.shape[0], _ptr(pos), _ptr(topk_w), T, H, k, _ptr(grad_y), _ptr(grad_w),
         _ptr(err_flag), _stream(stream)))
     return grad_y, grad_w
+
+
+_DTYPES = {"bf16": EP_DTYPE_BF16, "fp8": EP_DTYPE_FP8_E4M3_B128, "mxfp8": EP_DTYPE_MXFP8_E4M3_B32}
+
+
+def ep_decode_dispatch(scores, bias, cfg, experts_per_rank, x, dtype="bf16", topk_idx=None, topk_w=None, out=None,
+                       recv=None, recv_scales=None, err_flag=None, workspace=None, stream=None):
+    """Fused gate + layout + dispatch for decode-sized batches (T*k <= 4096)
+    in one launch.  Returns (topk_idx, topk_w, Layout, recv, recv_scales)."""
+    lib = load()
+    _dev(scores, torch.float32, "scores")
+    _dev(x, torch.bfloat16, "x")
+    T, E = scores.shape
+    k, H = cfg.top_k, x.shape[1]
+    d = scores.device
+    if bias is not None:
+        _dev(bias, torch.float32, "bias", (E,))
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=d)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=d)
+    if out is None:
+        out = alloc_layout(T, k, E, experts_per_rank, d)
+    code = _DTYPES[dtype]
+    if recv is None:
+        recv = torch.empty((T * k, H), dtype=torch.bfloat16 if dtype == "bf16" else torch.uint8, device=d)
+    if recv_scales is None and dtype != "bf16":
+        recv_scales = (torch.empty((recv.shape[0], H // 128), dtype=torch.float32, device=d) if dtype == "fp8"
+                       else torch.empty((recv.shape[0], H // 32), dtype=torch.uint8, device=d))
+    if workspace is None:
+        workspace = torch.zeros(64, dtype=torch.uint8, device=d)
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_decode_dispatch", lib.ep_decode_dispatch(
+        _ptr(scores), _ptr(bias), T, ctypes.byref(cfg), experts_per_rank, _ptr(x), H, code, _ptr(topk_idx),
+        _ptr(topk_w), _ptr(out.expert_count), _ptr(out.expert_off), _ptr(out.rank_count), _ptr(out.rank_off),
+        _ptr(out.rank_tokens), _ptr(out.pos), _ptr(out.src), _ptr(recv), recv.shape[0], _ptr(recv_scales),
+        _ptr(err_flag), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, out, recv, recv_scales
+
+
+def ep_selftest_grid_barrier(missing_arrivals, spin_limit, err_flag, workspace=None, stream=None):
+    """Runs the fused path's grid barrier alone (see include/ep.h)."""
+    lib = load()
+    _dev(err_flag, torch.int32, "err_flag")
+    if workspace is None:
+        workspace = torch.zeros(64, dtype=torch.uint8, device=err_flag.device)
+    _check("ep_selftest_grid_barrier", lib.ep_selftest_grid_barrier(int(missing_arrivals), int(spin_limit),
+                                                                    _ptr(err_flag), _ptr(workspace),
+                                                                    workspace.numel(), _stream(stream)))

@@ -19,75 +19,13 @@
 // block's amax is a 3-step xor-shuffle max, the scale an IEEE fp32 division
 // by 448, each code an IEEE fp32 division then a round-to-nearest-even
 // saturating e4m3 conversion (cvt.rn.satfinite).
-#include "ep_internal.cuh"
+#include "dispatch_impl.cuh"
 
 namespace ep {
 
 namespace {
 
 constexpr int kDispThreads = 256;
-constexpr int kBf16Unroll = 4;   // 16-byte chunks per lane per item (BF16)
-
-// Receive rows of token t for the calling warp: slot `lane` in p0, slot
-// `lane + 32` in p1; -1 where the slot does not exist, is empty, or names a
-// row outside [0, rows) (flagged).
-__device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long long t, int k, long long rows,
-                                           int lane, int32_t *err_flag, int &p0, int &p1)
-{
-    p0 = -1;
-    p1 = -1;
-    if (lane < k)
-        p0 = __ldg(pos + t * k + lane);
-    if (lane + 32 < k)
-        p1 = __ldg(pos + t * k + lane + 32);
-    if (p0 >= rows || p1 >= rows) {
-        if (err_flag)
-            atomicOr(err_flag, 2);
-        if (p0 >= rows)
-            p0 = -1;
-        if (p1 >= rows)
-            p1 = -1;
-    }
-}
-
-__device__ __forceinline__ int slot_row(int p0, int p1, int j)
-{
-    const int a = __shfl_sync(kFullMask, p0, j & 31);
-    const int b = __shfl_sync(kFullMask, p1, j & 31);
-    return j < 32 ? a : b;
-}
-
-// Walks warp items (token, segment) grid-stride without a division per item.
-struct ItemWalk {
-    long long t;
-    int seg;
-    int segs;
-    long long T;
-    int step_seg;
-    long long step_t;
-
-    __device__ ItemWalk(long long T_, int segs_)
-    {
-        T = T_;
-        segs = segs_;
-        const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-        const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-        t = warp / segs;
-        seg = (int)(warp - t * segs);
-        step_t = nwarps / segs;
-        step_seg = (int)(nwarps - step_t * segs);
-    }
-    __device__ bool valid() const { return t < T; }
-    __device__ void next()
-    {
-        t += step_t;
-        seg += step_seg;
-        if (seg >= segs) {
-            seg -= segs;
-            ++t;
-        }
-    }
-};
 
 __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                                      int k, const int32_t *__restrict__ pos,
@@ -95,32 +33,10 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint1
                                                                      int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const int C = H / 8;  // 16-byte chunks per row
-    const int segs = (C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll);
-    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+    for (ItemWalk it(T, bf16_segs(H)); it.valid(); it.next()) {
         int p0, p1;
         token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        const uint16_t *xrow = x + (size_t)it.t * H;
-        const int c0 = it.seg * 32 * kBf16Unroll + lane;
-        uint4 v[kBf16Unroll];
-#pragma unroll
-        for (int u = 0; u < kBf16Unroll; ++u) {
-            const int c = c0 + 32 * u;
-            if (c < C)
-                v[u] = ld_stream16(xrow + (size_t)c * 8);
-        }
-        for (int j = 0; j < k; ++j) {
-            const int p = slot_row(p0, p1, j);
-            if (p < 0)
-                continue;
-            uint16_t *dst = recv + (size_t)p * H;
-#pragma unroll
-            for (int u = 0; u < kBf16Unroll; ++u) {
-                const int c = c0 + 32 * u;
-                if (c < C)
-                    st_plain16(dst + (size_t)c * 8, v[u]);
-            }
-        }
+        dispatch_bf16_item(x, H, k, it.t, it.seg, p0, p1, recv);
     }
 }
 
@@ -131,62 +47,10 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16
                                                                     int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
-    const int nb = H / 128;  // scales per row
-    const int segs = (C16 + 31) / 32;
-    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+    for (ItemWalk it(T, fp8_segs(H)); it.valid(); it.next()) {
         int p0, p1;
         token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        const uint16_t *xrow = x + (size_t)it.t * H;
-        const int c = it.seg * 32 + lane;
-        // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
-        const bool act = c < C16;
-        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-        if (act) {
-            a = ld_stream16(xrow + (size_t)c * 16);
-            b = ld_stream16(xrow + (size_t)c * 16 + 8);
-        }
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float f[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = bf16_lo(wv[i]);
-            f[2 * i + 1] = bf16_hi(wv[i]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-        const float s = __fdiv_rn(amax, 448.0f);
-        uint32_t q[4];
-        if (amax == 0.0f) {
-            // all zeros: keep each element's sign bit (bf16 bit 15 -> code bit 7)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w0 = wv[2 * i], w1 = wv[2 * i + 1];
-                q[i] = ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
-                       (w1 & 0x80000000u);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
-                const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
-                q[i] = lo | (hi << 16);
-            }
-        }
-        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-        for (int j = 0; j < k; ++j) {
-            const int p = slot_row(p0, p1, j);
-            if (p < 0 || !act)
-                continue;
-            st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
-            if ((c & 7) == 0)
-                recv_s[(size_t)p * nb + (c >> 3)] = s;
-        }
+        dispatch_fp8_item(x, H, k, it.t, it.seg, p0, p1, recv_q, recv_s);
     }
 }
 
@@ -203,55 +67,10 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_mxfp8_kernel(const uint
                                                                       int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const int C16 = H / 16;  // 16-column groups per row; 2 per 32-column block
-    const int nb = H / 32;   // scale bytes per row
-    const int segs = (C16 + 31) / 32;
-    for (ItemWalk it(T, segs); it.valid(); it.next()) {
+    for (ItemWalk it(T, fp8_segs(H)); it.valid(); it.next()) {
         int p0, p1;
         token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        const uint16_t *xrow = x + (size_t)it.t * H;
-        const int c = it.seg * 32 + lane;
-        const bool act = c < C16;  // C16 is even: lane pairs are wholly in or out
-        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-        if (act) {
-            a = ld_stream16(xrow + (size_t)c * 16);
-            b = ld_stream16(xrow + (size_t)c * 16 + 8);
-        }
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float f[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = bf16_lo(wv[i]);
-            f[2 * i + 1] = bf16_hi(wv[i]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        // floor(log2(amax)) from the exponent field; zero and fp32 subnormals
-        // (below 2^-126) land on the clamp -127.
-        const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-        int e = ef == 0 ? -127 : ef - 127 - 8;
-        e = e < -127 ? -127 : e;
-        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e in [-127, 119]
-        uint32_t q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = pack_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
-            const uint32_t hi = pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-            q[i] = lo | (hi << 16);
-        }
-        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-        const uint8_t eb = (uint8_t)(e + 127);
-        for (int j = 0; j < k; ++j) {
-            const int p = slot_row(p0, p1, j);
-            if (p < 0 || !act)
-                continue;
-            st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
-            if ((c & 1) == 0)
-                recv_e[(size_t)p * nb + (c >> 1)] = eb;
-        }
+        dispatch_mxfp8_item(x, H, k, it.t, it.seg, p0, p1, recv_q, recv_e);
     }
 }
 
@@ -279,7 +98,7 @@ cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const 
 {
     if (T == 0)
         return cudaSuccess;
-    const long long items = (long long)T * ((H / 16 + 31) / 32);
+    const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_mxfp8_kernel, g_mx_per_sm, items);
     dispatch_mxfp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
     return cudaGetLastError();
@@ -290,8 +109,7 @@ cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const i
 {
     if (T == 0)
         return cudaSuccess;
-    const int C = H / 8;
-    const long long items = (long long)T * ((C + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll));
+    const long long items = (long long)T * bf16_segs(H);
     const int grid = persistent_grid((const void *)dispatch_bf16_kernel, g_bf16_per_sm, items);
     dispatch_bf16_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv, rows, err_flag);
     return cudaGetLastError();
@@ -302,7 +120,7 @@ cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const in
 {
     if (T == 0)
         return cudaSuccess;
-    const long long items = (long long)T * ((H / 16 + 31) / 32);
+    const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, items);
     dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag);
     return cudaGetLastError();

@@ -1,0 +1,232 @@
+// dispatch_impl.cuh -- per-item bodies of the permute-scatter, shared by the
+// dispatch kernels and the fused low-latency decode kernel.
+//
+// "Expert Parallelism (Parallelisme d'experts)", section "Le pattern de
+// communication all-to-all", Phase 1 Dispatch; FP8 modes from "DeepEP de
+// DeepSeek ...", section "Support FP8 et MXFP8".  A warp item is one token's
+// row segment: 32 lanes x 16 bytes (x kBf16Unroll for BF16) of x.  Lane j of
+// the warp holds the token's j-th receive row in p0 (j + 32 in p1).
+#pragma once
+
+#include "ep_internal.cuh"
+
+namespace ep {
+
+constexpr int kBf16Unroll = 4;  // 16-byte chunks per lane per item (BF16)
+
+// Receive rows of token t for the calling warp: slot `lane` in p0, slot
+// `lane + 32` in p1; -1 where the slot does not exist, is empty, or names a
+// row outside [0, rows) (flagged).
+__device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long long t, int k, long long rows,
+                                           int lane, int32_t *err_flag, int &p0, int &p1)
+{
+    p0 = -1;
+    p1 = -1;
+    if (lane < k)
+        p0 = __ldg(pos + t * k + lane);
+    if (lane + 32 < k)
+        p1 = __ldg(pos + t * k + lane + 32);
+    if (p0 >= rows || p1 >= rows) {
+        if (err_flag)
+            atomicOr(err_flag, 2);
+        if (p0 >= rows)
+            p0 = -1;
+        if (p1 >= rows)
+            p1 = -1;
+    }
+}
+
+__device__ __forceinline__ int slot_row(int p0, int p1, int j)
+{
+    const int a = __shfl_sync(kFullMask, p0, j & 31);
+    const int b = __shfl_sync(kFullMask, p1, j & 31);
+    return j < 32 ? a : b;
+}
+
+// Walks warp items (token, segment) grid-stride without a division per item.
+struct ItemPos {
+    long long t;
+    int seg;
+};
+
+struct ItemWalk {
+    long long t;
+    int seg;
+    int segs;
+    long long T;
+    int step_seg;
+    long long step_t;
+
+    __device__ ItemWalk(long long T_, int segs_)
+    {
+        T = T_;
+        segs = segs_;
+        const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+        const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+        t = warp / segs;
+        seg = (int)(warp - t * segs);
+        step_t = nwarps / segs;
+        step_seg = (int)(nwarps - step_t * segs);
+    }
+    __device__ bool valid() const { return t < T; }
+    __device__ void next()
+    {
+        t += step_t;
+        seg += step_seg;
+        if (seg >= segs) {
+            seg -= segs;
+            ++t;
+        }
+    }
+};
+
+// Items per token row.
+__device__ __host__ __forceinline__ int bf16_segs(int H) { return (H / 8 + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll); }
+__device__ __host__ __forceinline__ int fp8_segs(int H) { return (H / 16 + 31) / 32; }
+
+// BF16: recv[p_j, seg] = x[t, seg] for the token's k rows.
+__device__ __forceinline__ void dispatch_bf16_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
+                                                   int p0, int p1, uint16_t *__restrict__ recv)
+{
+    const int lane = threadIdx.x & 31;
+    const int C = H / 8;  // 16-byte chunks per row
+    ItemPos it{t, seg};
+    const uint16_t *xrow = x + (size_t)it.t * H;
+    const int c0 = it.seg * 32 * kBf16Unroll + lane;
+    uint4 v[kBf16Unroll];
+#pragma unroll
+    for (int u = 0; u < kBf16Unroll; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < C)
+            v[u] = ld_stream16(xrow + (size_t)c * 8);
+    }
+    for (int j = 0; j < k; ++j) {
+        const int p = slot_row(p0, p1, j);
+        if (p < 0)
+            continue;
+        uint16_t *dst = recv + (size_t)p * H;
+#pragma unroll
+        for (int u = 0; u < kBf16Unroll; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < C)
+                st_plain16(dst + (size_t)c * 8, v[u]);
+        }
+    }
+}
+
+// FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.
+__device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
+                                                  int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                  float *__restrict__ recv_s)
+{
+    const int lane = threadIdx.x & 31;
+    const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
+    const int nb = H / 128;  // scales per row
+    ItemPos it{t, seg};
+    const uint16_t *xrow = x + (size_t)it.t * H;
+    const int c = it.seg * 32 + lane;
+    // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
+    const bool act = c < C16;
+    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    if (act) {
+        a = ld_stream16(xrow + (size_t)c * 16);
+        b = ld_stream16(xrow + (size_t)c * 16 + 8);
+    }
+    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(wv[i]);
+        f[2 * i + 1] = bf16_hi(wv[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint32_t q[4];
+    if (amax == 0.0f) {
+        // all zeros: keep each element's sign bit (bf16 bit 15 -> code bit 7)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w0 = wv[2 * i], w1 = wv[2 * i + 1];
+            q[i] = ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
+                   (w1 & 0x80000000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
+            const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
+            q[i] = lo | (hi << 16);
+        }
+    }
+    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+    for (int j = 0; j < k; ++j) {
+        const int p = slot_row(p0, p1, j);
+        if (p < 0 || !act)
+            continue;
+        st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
+        if ((c & 7) == 0)
+            recv_s[(size_t)p * nb + (c >> 3)] = s;
+    }
+}
+
+// MXFP8: two lanes per 32-column block, E8M0 scale byte.
+__device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,
+                                                    int seg, int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                    uint8_t *__restrict__ recv_e)
+{
+    const int lane = threadIdx.x & 31;
+    const int C16 = H / 16;  // 16-column groups per row; 2 per 32-column block
+    const int nb = H / 32;   // scale bytes per row
+    ItemPos it{t, seg};
+    const uint16_t *xrow = x + (size_t)it.t * H;
+    const int c = it.seg * 32 + lane;
+    const bool act = c < C16;  // C16 is even: lane pairs are wholly in or out
+    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    if (act) {
+        a = ld_stream16(xrow + (size_t)c * 16);
+        b = ld_stream16(xrow + (size_t)c * 16 + 8);
+    }
+    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(wv[i]);
+        f[2 * i + 1] = bf16_hi(wv[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    // floor(log2(amax)) from the exponent field; zero and fp32 subnormals
+    // (below 2^-126) land on the clamp -127.
+    const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+    int e = ef == 0 ? -127 : ef - 127 - 8;
+    e = e < -127 ? -127 : e;
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e in [-127, 119]
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = pack_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+        const uint32_t hi = pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+        q[i] = lo | (hi << 16);
+    }
+    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+    const uint8_t eb = (uint8_t)(e + 127);
+    for (int j = 0; j < k; ++j) {
+        const int p = slot_row(p0, p1, j);
+        if (p < 0 || !act)
+            continue;
+        st_plain16(recv_q + (size_t)p * H + (size_t)c * 16, qv);
+        if ((c & 1) == 0)
+            recv_e[(size_t)p * nb + (c >> 1)] = eb;
+    }
+}
+
+}  // namespace ep

@@ -69,10 +69,13 @@ const char *ep_status_str(ep_status s)
     return "unknown status";
 }
 
-ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg, int32_t *topk_idx,
-                  float *topk_w, void *stream)
+}  // extern "C"
+
+namespace {
+
+ep_status check_gate_cfg(const ep_gate_cfg *cfg)
 {
-    if (!cfg || T < 0)
+    if (!cfg)
         return EP_ERR_INVALID_ARG;
     const int E = cfg->num_experts, k = cfg->top_k, G = cfg->n_groups, Kg = cfg->topk_group;
     const int kin = cfg->topk_in_group;
@@ -86,7 +89,28 @@ ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_ga
         return EP_ERR_INVALID_ARG;
     if (E > kMaxGateExperts || k > kMaxGateK || G > kMaxGroups || kin > kMaxKin)
         return EP_ERR_UNSUPPORTED;
-    if ((int64_t)T * E >= (int64_t)1 << 40)
+    return EP_OK;
+}
+
+ep::GateParams gate_params(const ep_gate_cfg *cfg)
+{
+    return ep::GateParams{cfg->num_experts, cfg->top_k, cfg->n_groups, cfg->topk_group, cfg->topk_in_group,
+                          cfg->score_fn, cfg->normalize};
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg, int32_t *topk_idx,
+                  float *topk_w, void *stream)
+{
+    if (T < 0)
+        return EP_ERR_INVALID_ARG;
+    const ep_status c = check_gate_cfg(cfg);
+    if (c != EP_OK)
+        return c;
+    if ((int64_t)T * cfg->num_experts >= (int64_t)1 << 40)
         return EP_ERR_UNSUPPORTED;
     if (T == 0)
         return EP_OK;
@@ -94,8 +118,8 @@ ep_status ep_gate(const float *scores, const float *bias, int32_t T, const ep_ga
         return EP_ERR_INVALID_ARG;
     if (!aligned(scores, 4) || (bias && !aligned(bias, 4)) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
         return EP_ERR_ALIGNMENT;
-    ep::GateParams p{E, k, G, Kg, kin, cfg->score_fn, cfg->normalize};
-    return launched(ep::launch_gate(scores, bias, T, p, topk_idx, topk_w, static_cast<cudaStream_t>(stream)));
+    return launched(
+        ep::launch_gate(scores, bias, T, gate_params(cfg), topk_idx, topk_w, static_cast<cudaStream_t>(stream)));
 }
 
 size_t ep_layout_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t experts_per_rank)
@@ -267,6 +291,60 @@ ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_row
     return launched(ep::launch_combine_backward(static_cast<const uint16_t *>(grad_out),
                                                 static_cast<const uint16_t *>(y), y_rows, pos, topk_w, T, H, k,
                                                 static_cast<uint16_t *>(grad_y), grad_w, err_flag,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_decode_dispatch(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
+                             int32_t experts_per_rank, const void *x, int32_t H, int32_t dtype, int32_t *topk_idx,
+                             float *topk_w, int32_t *expert_count, int32_t *expert_off, int32_t *rank_count,
+                             int32_t *rank_off, int32_t *rank_tokens, int32_t *pos, int32_t *src, void *recv,
+                             int32_t recv_rows, void *recv_scales, int32_t *err_flag, void *workspace,
+                             size_t workspace_bytes, void *stream)
+{
+    if (T < 1 || H < 1 || recv_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    const ep_status c = check_gate_cfg(cfg);
+    if (c != EP_OK)
+        return c;
+    const int E = cfg->num_experts, k = cfg->top_k;
+    const ep_status l = check_layout_args(T, k, E, experts_per_rank);
+    if (l != EP_OK)
+        return l;
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128 && dtype != EP_DTYPE_MXFP8_E4M3_B32)
+        return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0 || (dtype == EP_DTYPE_FP8_E4M3_B128 && H % 128 != 0) ||
+        (dtype == EP_DTYPE_MXFP8_E4M3_B32 && H % 32 != 0))
+        return EP_ERR_UNSUPPORTED;
+    if ((size_t)T * k > ep::decode_max_entries())
+        return EP_ERR_UNSUPPORTED;  // the fused path is for decode-sized batches
+    if (!expert_count || !expert_off || !rank_count || !rank_off || !rank_tokens || !workspace ||
+        workspace_bytes < sizeof(unsigned))
+        return EP_ERR_INVALID_ARG;
+    if (!scores || !x || !topk_idx || !topk_w || !pos || !src ||
+        (recv_rows > 0 && (!recv || (dtype != EP_DTYPE_BF16 && !recv_scales))))
+        return EP_ERR_INVALID_ARG;
+    const void *p4[] = {scores, bias, topk_idx, topk_w, expert_count, expert_off, rank_count, rank_off, rank_tokens,
+                        pos,    src,  err_flag, workspace};
+    for (const void *q : p4)
+        if (q && !aligned(q, 4))
+            return EP_ERR_ALIGNMENT;
+    if (!aligned(x, 16) || !aligned(recv, 16))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_decode(scores, bias, T, gate_params(cfg), experts_per_rank,
+                                      static_cast<const uint16_t *>(x), H, dtype, topk_idx, topk_w, expert_count,
+                                      expert_off, rank_count, rank_off, rank_tokens, pos, src, recv, recv_scales,
+                                      recv_rows, err_flag, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_selftest_grid_barrier(int32_t missing_arrivals, int64_t spin_limit, int32_t *err_flag, void *workspace,
+                                   size_t workspace_bytes, void *stream)
+{
+    if (missing_arrivals < 0 || spin_limit < 1 || spin_limit > ((int64_t)1 << 24) || !err_flag || !workspace ||
+        workspace_bytes < sizeof(unsigned))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(err_flag, 4) || !aligned(workspace, 4))
+        return EP_ERR_ALIGNMENT;
+    return launched(ep::launch_barrier_selftest((unsigned)missing_arrivals, spin_limit, err_flag, workspace,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

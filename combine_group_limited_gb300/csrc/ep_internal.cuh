@@ -110,6 +110,15 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
                                     const float *w, int T, int H, int k, uint16_t *grad_y, float *grad_w,
                                     int32_t *err_flag, cudaStream_t st);
 
+size_t decode_max_entries();
+cudaError_t launch_decode(const float *scores, const float *bias, int T, const GateParams &gp, int epr,
+                          const uint16_t *x, int H, int dtype, int32_t *topk_idx, float *topk_w,
+                          int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                          int32_t *rank_tokens, int32_t *pos, int32_t *src, void *recv, void *recv_scales,
+                          long long rows, int32_t *err_flag, void *barrier_word, cudaStream_t st);
+cudaError_t launch_barrier_selftest(unsigned extra, long long spin_limit, int32_t *err_flag, void *barrier_word,
+                                    cudaStream_t st);
+
 int device_sm_count();
 
 }  // namespace ep

@@ -37,6 +37,8 @@
  *    skipped and a bit is OR-ed into *err_flag (a device int32, may be NULL):
  *      EP_FLAG_BAD_EXPERT  an expert index neither -1 nor in [0, E)
  *      EP_FLAG_BAD_ROW     a receive row outside the buffer's rows
+ *      EP_FLAG_TIMEOUT     a bounded device-side wait ran out (the fused
+ *                          decode path's grid barrier); that work stopped
  *  - bf16 tensors are raw 16-bit bfloat16 patterns, row-major.
  *  - T*k rows always suffice for a receive buffer (top-k picks k distinct
  *    experts per token), so buffers are sized without reading any count
@@ -62,7 +64,7 @@ typedef enum {
     EP_ERR_CUDA = 4         /* the CUDA runtime reported an error at launch */
 } ep_status;
 
-enum { EP_FLAG_BAD_EXPERT = 1, EP_FLAG_BAD_ROW = 2 };
+enum { EP_FLAG_BAD_EXPERT = 1, EP_FLAG_BAD_ROW = 2, EP_FLAG_TIMEOUT = 4 };
 
 typedef enum {
     EP_SCORE_RAW = 0,    /* scores are affinities used as given (e.g. sigmoid outputs) */
@@ -291,6 +293,45 @@ ep_status ep_dispatch_backward(const void *grad_recv, int32_t recv_rows, const i
 ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_rows, const int32_t *pos,
                               const float *topk_w, int32_t T, int32_t H, int32_t k, void *grad_y,
                               float *grad_w, int32_t *err_flag, void *stream);
+
+/*
+ * Fused low-latency path for decode-sized batches ("DeepEP de DeepSeek
+ * ...", section "Kernels low-latency dispatch et combine"; "Expert
+ * Parallelism ...": decode messages of 100 KB - 2 MB): ep_gate,
+ * ep_get_layout and ep_dispatch in ONE cooperative launch, with results
+ * identical to the three separate calls.
+ *
+ * Arguments as those calls (cfg as ep_gate; experts_per_rank and the layout
+ * outputs as ep_get_layout; x, H, dtype, recv, recv_rows, recv_scales as
+ * ep_dispatch).  1 <= T and T*k <= 4096 (larger batches use the separate
+ * calls: EP_ERR_UNSUPPORTED).  workspace: >= 4 bytes of device memory,
+ * 4-byte aligned, holding the grid barrier's counter (cleared by the call;
+ * calls sharing it must not overlap on the GPU).  The grid barrier between
+ * gating and layout waits at most about a second; if that ran out,
+ * EP_FLAG_TIMEOUT is set in *err_flag and the outputs are incomplete.
+ * A device without cooperative launch returns EP_ERR_CUDA.
+ */
+ep_status ep_decode_dispatch(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
+                             int32_t experts_per_rank, const void *x, int32_t H, int32_t dtype,
+                             int32_t *topk_idx, float *topk_w, int32_t *expert_count,
+                             int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+                             int32_t *rank_tokens, int32_t *pos, int32_t *src, void *recv,
+                             int32_t recv_rows, void *recv_scales, int32_t *err_flag, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * Check of the fused path's bounded grid barrier: one cooperative launch
+ * whose CTAs wait for missing_arrivals arrivals that never come (0: none
+ * missing, the barrier completes).  With missing_arrivals > 0 every CTA
+ * polls spin_limit times (1 <= spin_limit <= 2^24; each poll sleeps about
+ * 64 ns plus a global load), then sets EP_FLAG_TIMEOUT in *err_flag and
+ * returns -- the wait ends on its own and the context stays usable.
+ * workspace as ep_decode_dispatch.  The pages have no counterpart to this
+ * call; it exists so that the timeout path is tested on the GPU without a
+ * hang.
+ */
+ep_status ep_selftest_grid_barrier(int32_t missing_arrivals, int64_t spin_limit, int32_t *err_flag,
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Static description of a status code. */
 const char *ep_status_str(ep_status s);

@@ -151,3 +151,24 @@ def test_next_row_entry_points_host_checks(lib):
     assert cb(FAKE, FAKE, 128, FAKE, FAKE, 16, 7168, 0, FAKE, FAKE, None, None) == 1
     assert cb(FAKE, FAKE, 128, FAKE, FAKE, 16, 7168, 8, ODD, FAKE, None, None) == 3
     assert cb(FAKE, None, 128, FAKE, FAKE, 16, 7168, 8, FAKE, FAKE, None, None) == 1
+
+
+def test_decode_entry_points_host_checks(lib):
+    import combine_group_limited_gb300 as ep
+    cfg = _cfg(ep)
+    dd = lambda T, H=7168, dtype=1, ws=FAKE, wsb=64, c=cfg: lib.ep_decode_dispatch(  # noqa: E731
+        FAKE, None, T, ctypes.byref(c), 8, FAKE, H, dtype, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+        FAKE, T * 8, FAKE, None, ws, wsb, None)
+    assert dd(0) == 1                                  # the fused path needs a token
+    assert dd(1000) == 2                               # T*k > 4096: use the separate calls
+    assert dd(128, H=7232) == 2                        # FP8 needs H % 128
+    assert dd(128, dtype=7) == 1
+    assert dd(128, ws=None) == 1
+    assert dd(128, wsb=2) == 1
+    assert dd(128, c=_cfg(ep, top_k=0)) == 1
+    sb = lib.ep_selftest_grid_barrier
+    assert sb(-1, 100, FAKE, FAKE, 64, None) == 1
+    assert sb(1, 0, FAKE, FAKE, 64, None) == 1
+    assert sb(1, (1 << 24) + 1, FAKE, FAKE, 64, None) == 1
+    assert sb(1, 100, None, FAKE, 64, None) == 1
+    assert sb(1, 100, ODD, ctypes.c_void_p(0x10001), 64, None) == 3
