@@ -16,9 +16,10 @@
 //
 // combine_fp8_kernel: the same reduction over FP8 expert outputs (e4m3 codes
 // with fp32 1x128 or E8M0 1x32 block scales).  A code converts exactly to
-// fp32 (cvt.rn.f16x2.e4m3x2, then f16 -> f32), times its block scale (exact
-// for E8M0 powers of two, one fp32 rounding for fp32 scales), then the same
-// fp32 fma chain in slot order.  2 bytes of FP8 payload per column per slot
+// fp32 (cvt.rn.f16x2.e4m3x2, then f16 -> f32); the slot's weight times its
+// block scale is formed once (exact for E8M0 powers of two, one fp32
+// rounding for fp32 scales) and the codes enter the same fp32 fma chain in
+// slot order.  2 bytes of FP8 payload per column per slot
 // instead of 2 bytes of BF16 halves the bytes the combine reads.
 #include <cuda_fp16.h>
 
@@ -147,16 +148,18 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
                 acc[i] = 0.0f;
             const int sb = kMx ? (c >> 1) : (c >> 3);  // this lane's scale block
             for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+                // First issue every load of the batch (codes and raw scale
+                // words), then convert: no load waits behind a conversion.
                 uint4 v[kSlotBatch];
-                float sc[kSlotBatch];
+                uint32_t sraw[kSlotBatch];
 #pragma unroll
                 for (int u = 0; u < kSlotBatch; ++u) {
                     const int j = j0 + u;
                     const int p = j < k ? s_pos[j] : -1;
                     if (p >= 0) {
                         v[u] = ld_stream16(yq + (size_t)p * H + (size_t)c * 16);
-                        sc[u] = kMx ? e8m0_to_f32(__ldg(static_cast<const uint8_t *>(yscale) + (size_t)p * nb + sb))
-                                    : __ldg(static_cast<const float *>(yscale) + (size_t)p * nb + sb);
+                        sraw[u] = kMx ? (uint32_t)__ldg(static_cast<const uint8_t *>(yscale) + (size_t)p * nb + sb)
+                                      : __float_as_uint(__ldg(static_cast<const float *>(yscale) + (size_t)p * nb + sb));
                     }
                 }
 #pragma unroll
@@ -164,16 +167,19 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
                     const int j = j0 + u;
                     const int p = j < k ? s_pos[j] : -1;
                     if (p >= 0) {
-                        const float wj = s_w[j];
+                        // weight times block scale once per slot: one fp32
+                        // rounding per term, as scaling each code would be
+                        const float sc = kMx ? e8m0_to_f32(sraw[u]) : __uint_as_float(sraw[u]);
+                        const float ws = s_w[j] * sc;
                         const uint32_t vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float d0, d1, d2, d3;
                             e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
-                            acc[4 * i] = fmaf(wj, d0 * sc[u], acc[4 * i]);
-                            acc[4 * i + 1] = fmaf(wj, d1 * sc[u], acc[4 * i + 1]);
-                            acc[4 * i + 2] = fmaf(wj, d2 * sc[u], acc[4 * i + 2]);
-                            acc[4 * i + 3] = fmaf(wj, d3 * sc[u], acc[4 * i + 3]);
+                            acc[4 * i] = fmaf(ws, d0, acc[4 * i]);
+                            acc[4 * i + 1] = fmaf(ws, d1, acc[4 * i + 1]);
+                            acc[4 * i + 2] = fmaf(ws, d2, acc[4 * i + 2]);
+                            acc[4 * i + 3] = fmaf(ws, d3, acc[4 * i + 3]);
                         }
                     }
                 }

@@ -293,8 +293,10 @@ cudaError_t launch_epl(DecodeArgs a, cudaStream_t st)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
-    // One CTA per SM: every CTA is resident, as the grid barrier requires.
-    const int grid = device_sm_count();
+    // At most the resident CTAs per SM (up to 3, for the scatter's bytes in
+    // flight) times the SMs: every CTA is resident, as the grid barrier
+    // requires (the cooperative launch refuses a larger grid).
+    const int grid = device_sm_count() * (per_sm < 3 ? per_sm : 3);
     e = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), st);
     if (e != cudaSuccess)
         return e;

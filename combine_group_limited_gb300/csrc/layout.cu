@@ -7,7 +7,8 @@
 // distinct experts fills at most T*k rows, so nothing here is read back to
 // the host.
 //
-// Three launches over tiles of whole tokens (about 512 entries each):
+// Batches of up to 16384 entries take one launch (layout_small_kernel); larger
+// ones take three launches over tiles of whole tokens (about 512 entries each):
 //  1. count:  per tile, per-expert entry counts and per-rank distinct-token
 //             counts (shared-memory integer atomics; the totals do not depend
 //             on their order).  Workspace columns [E][tiles], [R][tiles].
@@ -34,6 +35,9 @@ constexpr int kTileEntries = 512;
 constexpr int kPlaceThreads = 256;
 constexpr int kPlaceWarps = kPlaceThreads / 32;
 constexpr int kMaxExperts = 1024;
+constexpr int kSmallThreads = 512;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallEntries = 16384;  // single-launch layout up to this many entries
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return (unsigned)e < (unsigned)E; }
 
@@ -348,6 +352,149 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
     }
 }
 
+// Small batches (T*k <= kSmallEntries): the whole layout in one CTA and one
+// launch -- the three-launch path is latency-bound there.  Same results:
+// counts and distinct tokens by shared-memory atomics, an exclusive scan of
+// the counts, then stable rows from 16 warps taking contiguous slices in
+// flat order (__match_any_sync ranks inside 32-entry chunks, per-warp
+// running counts based on the lower warps' counts).
+__global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
+    const int32_t *__restrict__ idx, int T, int k, int E, int epr, int32_t *__restrict__ expert_count,
+    int32_t *__restrict__ expert_off, int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_off,
+    int32_t *__restrict__ rank_tokens, int32_t *__restrict__ pos, int32_t *__restrict__ src,
+    int32_t *__restrict__ err_flag)
+{
+    extern __shared__ int32_t ssm[];  // off [E], rank tokens [R], hist [kSmallWarps][E]
+    const int R = E / epr;
+    const int N = T * k;
+    int32_t *s_off = ssm;
+    int32_t *s_rt = s_off + E;
+    int32_t *hist = s_rt + R;
+    __shared__ int32_t s_wsum[kSmallWarps];
+    __shared__ int32_t s_total;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < E + R + kSmallWarps * E; i += blockDim.x)
+        ssm[i] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const int e = __ldg(idx + i);
+        if (!valid_expert(e, E)) {
+            bad |= e != -1;
+            continue;
+        }
+        atomicAdd(&s_off[e], 1);
+        const int r = e / epr;
+        const int j = i % k;
+        bool first = true;
+        for (int jj = 0; jj < j; ++jj) {
+            const int e2 = __ldg(idx + i - j + jj);
+            first &= !(valid_expert(e2, E) && e2 / epr == r);
+        }
+        if (first)
+            atomicAdd(&s_rt[r], 1);
+    }
+    if (bad && err_flag)
+        atomicOr(err_flag, 1);
+    __syncthreads();
+    {
+        constexpr int kPerThread = kMaxExperts / kSmallThreads;
+        const int e0 = threadIdx.x * kPerThread;
+        int v[kPerThread];
+        int sum = 0;
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            v[u] = e0 + u < E ? s_off[e0 + u] : 0;
+            sum += v[u];
+        }
+        const int incl = warp_incl_scan(sum, lane);
+        if (lane == 31)
+            s_wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int ws = lane < kSmallWarps ? s_wsum[lane] : 0;
+            const int wi = warp_incl_scan(ws, lane);
+            if (lane < kSmallWarps)
+                s_wsum[lane] = wi - ws;
+        }
+        __syncthreads();
+        int run = s_wsum[warp] + incl - sum;
+#pragma unroll
+        for (int u = 0; u < kPerThread; ++u) {
+            if (e0 + u < E) {
+                s_off[e0 + u] = run;
+                expert_count[e0 + u] = v[u];
+                expert_off[e0 + u] = run;
+            }
+            if (e0 + u == E - 1)
+                s_total = run + v[u];
+            run += v[u];
+        }
+    }
+    __syncthreads();
+    const int total = s_total;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const int lo = s_off[r * epr];
+        const int hi = (r + 1) * epr < E ? s_off[(r + 1) * epr] : total;
+        rank_off[r] = lo;
+        rank_count[r] = hi - lo;
+        rank_tokens[r] = s_rt[r];
+    }
+    if (threadIdx.x == 0) {
+        expert_off[E] = total;
+        rank_off[R] = total;
+    }
+    for (int i = total + threadIdx.x; i < N; i += blockDim.x)
+        src[i] = -1;
+
+    const int per_warp = ((N + kSmallWarps * 32 - 1) / (kSmallWarps * 32)) * 32;
+    const int w0 = warp * per_warp;
+    const int w1 = min(N, w0 + per_warp);
+    int32_t *my = hist + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int c = w0; c < w1; c += 32) {
+        const int i = c + lane;
+        const int e = i < w1 ? __ldg(idx + i) : -1;
+        const int key = valid_expert(e, E) ? e : E;
+        const unsigned grp = __match_any_sync(kFullMask, key);
+        if (key < E && lane == __ffs(grp) - 1)
+            my[key] += __popc(grp);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int base = s_off[e];
+        for (int w = 0; w < kSmallWarps; ++w) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = base;
+            base += c;
+        }
+    }
+    __syncthreads();
+    for (int c = w0; c < w1; c += 32) {
+        const int i = c + lane;
+        const bool in = i < w1;
+        const int e = in ? __ldg(idx + i) : -1;
+        const int key = valid_expert(e, E) ? e : E;
+        const unsigned grp = __match_any_sync(kFullMask, key);
+        if (key < E) {
+            const int p = my[key] + __popc(grp & lt_mask);
+            if (p >= 0 && p < N) {
+                pos[i] = p;
+                src[p] = i;
+            } else {
+                pos[i] = -1;
+            }
+        } else if (in) {
+            pos[i] = -1;
+        }
+        __syncwarp();
+        if (key < E && lane == __ffs(grp) - 1)
+            my[key] += __popc(grp);
+        __syncwarp();
+    }
+}
+
 // Zero counts for an empty batch (no tile runs).
 __global__ void layout_empty_kernel(int E, int epr, int cap, int32_t *expert_count, int32_t *expert_off,
                                     int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
@@ -411,6 +558,23 @@ cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int
     if (nt == 0) {
         layout_empty_kernel<<<1, 256, 0, st>>>(E, epr, cap, expert_count, expert_off, rank_count, rank_off,
                                                rank_tokens, expert_dropped);
+        return cudaGetLastError();
+    }
+    if (!capped && T * k <= kSmallEntries) {
+        const size_t smem = ((size_t)E + R + (size_t)kSmallWarps * E) * sizeof(int32_t);
+        if (smem > 48 * 1024) {
+            static bool attr_set = false;
+            if (!attr_set) {
+                cudaError_t e = cudaFuncSetAttribute((const void *)layout_small_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)(((size_t)kMaxExperts * (kSmallWarps + 2)) * sizeof(int32_t)));
+                if (e != cudaSuccess)
+                    return e;
+                attr_set = true;
+            }
+        }
+        layout_small_kernel<<<1, kSmallThreads, smem, st>>>(topk_idx, T, k, E, epr, expert_count, expert_off,
+                                                            rank_count, rank_off, rank_tokens, pos, src, err_flag);
         return cudaGetLastError();
     }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
