@@ -11,9 +11,9 @@
 //   2. a grid barrier (every CTA is resident: cooperative launch), with a
 //      bounded wait -- past its limit a CTA sets EP_FLAG_TIMEOUT and stops;
 //   3. every CTA rebuilds the whole layout of the T*k <= 4096 entries in
-//      shared memory (histogram, exclusive scan, stable ranks by
-//      __match_any_sync) from the chosen experts; CTA 0 writes the layout
-//      outputs;
+//      shared memory (warp-aggregated histogram, exclusive scan, stable
+//      ranks from ballot peer masks) from the chosen experts; CTA 0 writes
+//      the layout outputs;
 //   4. warp items over (token, row segment) grid-wide scatter the rows
 //      (dispatch_impl.cuh), reading each token's receive rows from shared
 //      memory.
@@ -116,10 +116,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
     for (int i = threadIdx.x; i < E + kDecWarps * E + R; i += blockDim.x)
         s_off[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        const int e = s_idx[i];
-        if ((unsigned)e < (unsigned)E)
-            atomicAdd(&s_off[e], 1);
+    const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
+    for (int base = threadIdx.x & ~31; base < N; base += blockDim.x) {
+        const int i = base + lane;
+        const int e = i < N ? s_idx[i] : -1;
+        const bool ok = (unsigned)e < (unsigned)E;
+        warp_count(s_off, ok ? (unsigned)e : 0u, ok, eb);
     }
     __syncthreads();
     {
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
         const int i = c + lane;
         const int e = i < w1 ? s_idx[i] : -1;
         const int key = (unsigned)e < (unsigned)E ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E && lane == __ffs(grp) - 1)
             my[key] += __popc(grp);
         __syncwarp();
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
         const bool in = i < w1;
         const int e = in ? s_idx[i] : -1;
         const int key = (unsigned)e < (unsigned)E ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         if (in)
             s_pos[i] = key < E ? my[key] + __popc(grp & lt_mask) : -1;
         __syncwarp();
@@ -209,24 +211,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
             a.expert_off[E] = total;
             a.rank_off[R] = total;
         }
-        for (int i = threadIdx.x; i < N; i += blockDim.x) {
-            const int p = s_pos[i];
-            a.pos[i] = p;
-            if (p >= 0)
-                a.src[p] = i;
-            const int e = s_idx[i];
-            if ((unsigned)e < (unsigned)E) {
-                // distinct tokens per rank: the token's first slot on the rank counts
-                const int r = e / a.epr;
+        for (int base = threadIdx.x & ~31; base < N; base += blockDim.x) {
+            const int i = base + lane;
+            const bool in = i < N;
+            const int p = in ? s_pos[i] : -1;
+            if (in) {
+                a.pos[i] = p;
+                if (p >= 0)
+                    a.src[p] = i;
+            }
+            const int e = in ? s_idx[i] : -1;
+            const bool ok = (unsigned)e < (unsigned)E;
+            // distinct tokens per rank: the token's first slot on the rank counts
+            const int r = ok ? e / a.epr : 0;
+            bool first = ok;
+            if (ok) {
                 const int j = i % k;
-                bool first = true;
                 for (int jj = 0; jj < j; ++jj) {
                     const int e2 = s_idx[i - j + jj];
                     first &= !((unsigned)e2 < (unsigned)E && e2 / a.epr == r);
                 }
-                if (first)
-                    atomicAdd(&s_rt[r], 1);
             }
+            warp_count(s_rt, (unsigned)r, first, rb);
         }
         for (int i = total + threadIdx.x; i < N; i += blockDim.x)
             a.src[i] = -1;

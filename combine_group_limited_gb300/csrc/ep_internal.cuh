@@ -70,6 +70,39 @@ __device__ __forceinline__ void st_plain16(void *p, uint4 v)
                  : "memory");
 }
 
+// Lanes of the warp whose key equals this lane's key, for keys in
+// [0, 2^nbits): one ballot per key bit (every lane must call it).  Unlike
+// __match_any_sync its cost does not grow with the number of distinct keys.
+__device__ __forceinline__ unsigned peer_mask(unsigned key, int nbits)
+{
+    unsigned m = kFullMask;
+    for (int b = 0; b < nbits; ++b) {
+        const unsigned bit = (key >> b) & 1u;
+        const unsigned bal = __ballot_sync(kFullMask, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
+// Bits needed for keys 0..max_key.
+__host__ __device__ __forceinline__ int key_bits(unsigned max_key)
+{
+    int b = 1;
+    while ((max_key >> b) != 0u)
+        ++b;
+    return b;
+}
+
+// Warp-aggregated shared-memory increment of cnt[key] for the active lanes
+// (every lane must call it; inactive lanes pass any key).
+__device__ __forceinline__ void warp_count(int32_t *cnt, unsigned key, bool active, int nbits)
+{
+    const unsigned act = __ballot_sync(kFullMask, active);
+    const unsigned peers = peer_mask(key, nbits) & act;
+    if (active && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1))
+        atomicAdd(&cnt[key], __popc(peers));
+}
+
 struct GateParams {
     int E, k, G, Kg, kin, score_fn, normalize;
 };

@@ -17,7 +17,7 @@
 //  3. place:  every CTA scans the E expert totals itself (a block scan of at
 //             most 1024 values, 4 per thread) to get expert_off, then gives each entry its
 //             stable row: 8 warps take contiguous slices in flat order;
-//             __match_any_sync groups equal experts inside a 32-entry chunk,
+//             a ballot per key bit groups equal experts inside a 32-entry chunk,
 //             so an entry's row is its expert's offset + the tile's base + the
 //             lower warps' counts + the running count of its warp + the
 //             popcount of lower lanes in its group -- the order a sequential
@@ -56,32 +56,34 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(
     const int tile = blockIdx.x;
     const int n0 = tile * tile_tok * k;
     const int n1 = min(T, (tile + 1) * tile_tok) * k;
+    const int lane = threadIdx.x & 31;
+    const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
     int bad = 0;
-    for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
-        const int e = __ldg(idx + i);
-        int r = -1;
-        if (valid_expert(e, E)) {
-            atomicAdd(&cnt_smem[e], 1);
-            r = e / epr;
-        } else if (e != -1) {
-            bad = 1;
-        }
-        s_rank[i - n0] = r;
+    // Warp-uniform loops: the counts are warp-aggregated (warp_count).
+    for (int base = n0 + (threadIdx.x & ~31); base < n1; base += blockDim.x) {
+        const int i = base + lane;
+        const bool in = i < n1;
+        const int e = in ? __ldg(idx + i) : -1;
+        const bool ok = valid_expert(e, E);
+        bad |= in && !ok && e != -1;
+        warp_count(cnt_smem, ok ? (unsigned)e : 0u, ok, eb);
+        if (in)
+            s_rank[i - n0] = ok ? e / epr : -1;
     }
     __syncthreads();
     // Distinct tokens per rank: an entry counts if no earlier slot of its
     // token is on the same rank.
-    for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
-        const int r = s_rank[i - n0];
-        if (r < 0)
-            continue;
-        const int j = (i - n0) % k;
-        const int32_t *tok = s_rank + (i - n0 - j);
-        bool first = true;
-        for (int jj = 0; jj < j; ++jj)
-            first &= tok[jj] != r;
-        if (first)
-            atomicAdd(&cnt_smem[E + r], 1);
+    for (int base = n0 + (threadIdx.x & ~31); base < n1; base += blockDim.x) {
+        const int i = base + lane;
+        const int r = i < n1 ? s_rank[i - n0] : -1;
+        bool first = r >= 0;
+        if (first) {
+            const int j = (i - n0) % k;
+            const int32_t *tok = s_rank + (i - n0 - j);
+            for (int jj = 0; jj < j; ++jj)
+                first &= tok[jj] != r;
+        }
+        warp_count(cnt_smem + E, first ? (unsigned)r : 0u, first, rb);
     }
     if (bad && err_flag)
         atomicOr(err_flag, (int)1);
@@ -270,13 +272,14 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
     const int w1 = min(n1, w0 + per_warp);
     int32_t *my = hist + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
+    const int eb = key_bits((unsigned)E);  // keys 0..E (E marks an invalid entry)
 
     // A: each warp's per-expert counts.
     for (int c = w0; c < w1; c += 32) {
         const int i = c + lane;
         const int e = i < w1 ? __ldg(idx + i) : -1;
         const int key = valid_expert(e, E) ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E && lane == __ffs(grp) - 1)
             my[key] += __popc(grp);
         __syncwarp();
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
         const bool in = i < w1;
         const int e = in ? __ldg(idx + i) : -1;
         const int key = valid_expert(e, E) ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         int kept_rank = -1;
         if (key < E) {
             const int r = my[key] + __popc(grp & lt_mask);
@@ -333,17 +336,18 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
     if (kCap) {
         // Distinct tokens with a kept entry, per rank.
         __syncthreads();
-        for (int i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
-            const int r = s_krank[i - n0];
-            if (r < 0)
-                continue;
-            const int j = (i - n0) % k;
-            const int32_t *tok = s_krank + (i - n0 - j);
-            bool first = true;
-            for (int jj = 0; jj < j; ++jj)
-                first &= tok[jj] != r;
-            if (first)
-                atomicAdd(&s_rt[r], 1);
+        const int rb = key_bits((unsigned)R);
+        for (int base = n0 + (threadIdx.x & ~31); base < n1; base += blockDim.x) {
+            const int i = base + lane;
+            const int r = i < n1 ? s_krank[i - n0] : -1;
+            bool first = r >= 0;
+            if (first) {
+                const int j = (i - n0) % k;
+                const int32_t *tok = s_krank + (i - n0 - j);
+                for (int jj = 0; jj < j; ++jj)
+                    first &= tok[jj] != r;
+            }
+            warp_count(s_rt, first ? (unsigned)r : 0u, first, rb);
         }
         __syncthreads();
         for (int r = threadIdx.x; r < R; r += blockDim.x)
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
 // launch -- the three-launch path is latency-bound there.  Same results:
 // counts and distinct tokens by shared-memory atomics, an exclusive scan of
 // the counts, then stable rows from 16 warps taking contiguous slices in
-// flat order (__match_any_sync ranks inside 32-entry chunks, per-warp
+// flat order (ballot peer masks rank inside 32-entry chunks, per-warp
 // running counts based on the lower warps' counts).
 __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
     const int32_t *__restrict__ idx, int T, int k, int E, int epr, int32_t *__restrict__ expert_count,
@@ -377,22 +381,23 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         ssm[i] = 0;
     __syncthreads();
     int bad = 0;
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        const int e = __ldg(idx + i);
-        if (!valid_expert(e, E)) {
-            bad |= e != -1;
-            continue;
+    const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
+    for (int base = threadIdx.x & ~31; base < N; base += blockDim.x) {
+        const int i = base + lane;
+        const int e = i < N ? __ldg(idx + i) : -1;
+        const bool ok = valid_expert(e, E);
+        bad |= i < N && !ok && e != -1;
+        warp_count(s_off, ok ? (unsigned)e : 0u, ok, eb);
+        const int r = ok ? e / epr : 0;
+        bool first = ok;
+        if (ok) {
+            const int j = i % k;
+            for (int jj = 0; jj < j; ++jj) {
+                const int e2 = __ldg(idx + i - j + jj);
+                first &= !(valid_expert(e2, E) && e2 / epr == r);
+            }
         }
-        atomicAdd(&s_off[e], 1);
-        const int r = e / epr;
-        const int j = i % k;
-        bool first = true;
-        for (int jj = 0; jj < j; ++jj) {
-            const int e2 = __ldg(idx + i - j + jj);
-            first &= !(valid_expert(e2, E) && e2 / epr == r);
-        }
-        if (first)
-            atomicAdd(&s_rt[r], 1);
+        warp_count(s_rt, (unsigned)r, first, rb);
     }
     if (bad && err_flag)
         atomicOr(err_flag, 1);
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         const int i = c + lane;
         const int e = i < w1 ? __ldg(idx + i) : -1;
         const int key = valid_expert(e, E) ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E && lane == __ffs(grp) - 1)
             my[key] += __popc(grp);
         __syncwarp();
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         const bool in = i < w1;
         const int e = in ? __ldg(idx + i) : -1;
         const int key = valid_expert(e, E) ? e : E;
-        const unsigned grp = __match_any_sync(kFullMask, key);
+        const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E) {
             const int p = my[key] + __popc(grp & lt_mask);
             if (p >= 0 && p < N) {
