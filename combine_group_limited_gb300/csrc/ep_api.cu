@@ -318,7 +318,7 @@ ep_status ep_decode_dispatch(const float *scores, const float *bias, int32_t T, 
     if ((size_t)T * k > ep::decode_max_entries())
         return EP_ERR_UNSUPPORTED;  // the fused path is for decode-sized batches
     if (!expert_count || !expert_off || !rank_count || !rank_off || !rank_tokens || !workspace ||
-        workspace_bytes < sizeof(unsigned))
+        workspace_bytes < 2 * sizeof(unsigned))
         return EP_ERR_INVALID_ARG;
     if (!scores || !x || !topk_idx || !topk_w || !pos || !src ||
         (recv_rows > 0 && (!recv || (dtype != EP_DTYPE_BF16 && !recv_scales))))
@@ -340,7 +340,7 @@ ep_status ep_selftest_grid_barrier(int32_t missing_arrivals, int64_t spin_limit,
                                    size_t workspace_bytes, void *stream)
 {
     if (missing_arrivals < 0 || spin_limit < 1 || spin_limit > ((int64_t)1 << 24) || !err_flag || !workspace ||
-        workspace_bytes < sizeof(unsigned))
+        workspace_bytes < 2 * sizeof(unsigned))
         return EP_ERR_INVALID_ARG;
     if (!aligned(err_flag, 4) || !aligned(workspace, 4))
         return EP_ERR_ALIGNMENT;

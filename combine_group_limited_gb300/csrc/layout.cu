@@ -7,7 +7,7 @@
 // distinct experts fills at most T*k rows, so nothing here is read back to
 // the host.
 //
-// Batches of up to 16384 entries take one launch (layout_small_kernel); larger
+// Batches of up to 4096 entries take one launch (layout_small_kernel); larger
 // ones take three launches over tiles of whole tokens (about 512 entries each):
 //  1. count:  per tile, per-expert entry counts and per-rank distinct-token
 //             counts (shared-memory integer atomics; the totals do not depend
@@ -37,7 +37,8 @@ constexpr int kPlaceWarps = kPlaceThreads / 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kSmallThreads = 512;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallEntries = 16384;  // single-launch layout up to this many entries
+constexpr int kSmallEntries = 4096;  // single-launch layout up to this many entries
+constexpr int kSmallChunks = kSmallEntries / (kSmallWarps * 32);  // 32-entry chunks per warp
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return (unsigned)e < (unsigned)E; }
 
@@ -357,50 +358,72 @@ __global__ void __launch_bounds__(kPlaceThreads) layout_place_kernel(
 }
 
 // Small batches (T*k <= kSmallEntries): the whole layout in one CTA and one
-// launch -- the three-launch path is latency-bound there.  Same results:
-// counts and distinct tokens by shared-memory atomics, an exclusive scan of
-// the counts, then stable rows from 16 warps taking contiguous slices in
-// flat order (ballot peer masks rank inside 32-entry chunks, per-warp
-// running counts based on the lower warps' counts).
+// launch -- the three-launch path is latency-bound there.  Same results.
+// Each warp owns a contiguous slice of at most kSmallChunks x 32 entries and
+// loads it into registers once (no load waits inside the passes): counts and
+// distinct tokens by warp-aggregated shared counters, an exclusive scan of
+// the counts, then stable rows -- ballot peer masks rank equal experts inside
+// a 32-entry chunk, per-warp running counts start at the lower warps' counts.
 __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
     const int32_t *__restrict__ idx, int T, int k, int E, int epr, int32_t *__restrict__ expert_count,
     int32_t *__restrict__ expert_off, int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_off,
     int32_t *__restrict__ rank_tokens, int32_t *__restrict__ pos, int32_t *__restrict__ src,
     int32_t *__restrict__ err_flag)
 {
-    extern __shared__ int32_t ssm[];  // off [E], rank tokens [R], hist [kSmallWarps][E]
+    extern __shared__ int32_t ssm[];  // off [E], rank tokens [R], hist [kSmallWarps][E], ranks [N]
     const int R = E / epr;
     const int N = T * k;
     int32_t *s_off = ssm;
     int32_t *s_rt = s_off + E;
     int32_t *hist = s_rt + R;
+    int32_t *s_rank = hist + kSmallWarps * E;
     __shared__ int32_t s_wsum[kSmallWarps];
     __shared__ int32_t s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < E + R + kSmallWarps * E; i += blockDim.x)
         ssm[i] = 0;
+    const int per_warp = ((N + kSmallWarps * 32 - 1) / (kSmallWarps * 32)) * 32;  // <= kSmallChunks * 32
+    const int w0 = warp * per_warp;
+    int ev[kSmallChunks];
+#pragma unroll
+    for (int c = 0; c < kSmallChunks; ++c) {
+        const int i = w0 + 32 * c + lane;
+        ev[c] = (32 * c < per_warp && i < N) ? __ldg(idx + i) : -2;  // -2: outside the slice
+    }
     __syncthreads();
-    int bad = 0;
     const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
-    for (int base = threadIdx.x & ~31; base < N; base += blockDim.x) {
-        const int i = base + lane;
-        const int e = i < N ? __ldg(idx + i) : -1;
+    int bad = 0;
+#pragma unroll
+    for (int c = 0; c < kSmallChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int i = w0 + 32 * c + lane;
+        const int e = ev[c];
         const bool ok = valid_expert(e, E);
-        bad |= i < N && !ok && e != -1;
+        bad |= e != -2 && e != -1 && !ok;
         warp_count(s_off, ok ? (unsigned)e : 0u, ok, eb);
-        const int r = ok ? e / epr : 0;
-        bool first = ok;
-        if (ok) {
-            const int j = i % k;
-            for (int jj = 0; jj < j; ++jj) {
-                const int e2 = __ldg(idx + i - j + jj);
-                first &= !(valid_expert(e2, E) && e2 / epr == r);
-            }
-        }
-        warp_count(s_rt, (unsigned)r, first, rb);
+        if (e != -2)
+            s_rank[i] = ok ? e / epr : -1;
     }
     if (bad && err_flag)
         atomicOr(err_flag, 1);
+    __syncthreads();
+    // Distinct tokens per rank: an entry counts if no earlier slot of its
+    // token is on the same rank (ranks read from shared memory).
+#pragma unroll
+    for (int c = 0; c < kSmallChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int i = w0 + 32 * c + lane;
+        const int r = (ev[c] != -2) ? s_rank[i] : -1;
+        bool first = r >= 0;
+        if (first) {
+            const int j = i % k;
+            for (int jj = 0; jj < j; ++jj)
+                first &= s_rank[i - j + jj] != r;
+        }
+        warp_count(s_rt, first ? (unsigned)r : 0u, first, rb);
+    }
     __syncthreads();
     {
         constexpr int kPerThread = kMaxExperts / kSmallThreads;
@@ -452,14 +475,13 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
     for (int i = total + threadIdx.x; i < N; i += blockDim.x)
         src[i] = -1;
 
-    const int per_warp = ((N + kSmallWarps * 32 - 1) / (kSmallWarps * 32)) * 32;
-    const int w0 = warp * per_warp;
-    const int w1 = min(N, w0 + per_warp);
     int32_t *my = hist + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int c = w0; c < w1; c += 32) {
-        const int i = c + lane;
-        const int e = i < w1 ? __ldg(idx + i) : -1;
+#pragma unroll
+    for (int c = 0; c < kSmallChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int e = ev[c];
         const int key = valid_expert(e, E) ? e : E;
         const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E && lane == __ffs(grp) - 1)
@@ -476,10 +498,12 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         }
     }
     __syncthreads();
-    for (int c = w0; c < w1; c += 32) {
-        const int i = c + lane;
-        const bool in = i < w1;
-        const int e = in ? __ldg(idx + i) : -1;
+#pragma unroll
+    for (int c = 0; c < kSmallChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int i = w0 + 32 * c + lane;
+        const int e = ev[c];
         const int key = valid_expert(e, E) ? e : E;
         const unsigned grp = peer_mask((unsigned)key, eb);
         if (key < E) {
@@ -490,7 +514,7 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
             } else {
                 pos[i] = -1;
             }
-        } else if (in) {
+        } else if (e == -1 || (e != -2 && i < N)) {
             pos[i] = -1;
         }
         __syncwarp();
@@ -566,13 +590,13 @@ cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int
         return cudaGetLastError();
     }
     if (!capped && T * k <= kSmallEntries) {
-        const size_t smem = ((size_t)E + R + (size_t)kSmallWarps * E) * sizeof(int32_t);
+        const size_t smem = ((size_t)E + R + (size_t)kSmallWarps * E + (size_t)T * k) * sizeof(int32_t);
         if (smem > 48 * 1024) {
             static bool attr_set = false;
             if (!attr_set) {
-                cudaError_t e = cudaFuncSetAttribute((const void *)layout_small_kernel,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)(((size_t)kMaxExperts * (kSmallWarps + 2)) * sizeof(int32_t)));
+                cudaError_t e = cudaFuncSetAttribute(
+                    (const void *)layout_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    (int)(((size_t)kMaxExperts * (kSmallWarps + 2) + kSmallEntries) * sizeof(int32_t)));
                 if (e != cudaSuccess)
                     return e;
                 attr_set = true;

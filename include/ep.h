@@ -236,10 +236,10 @@ ep_status ep_combine(const void *y, int32_t y_rows, const int32_t *pos, const fl
  * yscales      scale_dtype EP_DTYPE_FP8_E4M3_B128: fp32 [y_rows, H/128];
  *              EP_DTYPE_MXFP8_E4M3_B32: E8M0 bytes [y_rows, H/32].
  * pos, topk_w, out, err_flag as in ep_combine.
- * out[t, h] = bf16_rne( fp32 fma chain over j of w[t,j] * (e4m3 value of
- * yq[pos[t,j], h] * its block scale) ), the dequantised product taken in
- * fp32.  Errors as ep_combine, plus EP_ERR_UNSUPPORTED when H is not a
- * multiple of the block width.
+ * out[t, h] = bf16_rne( fp32 fma chain over j of (w[t,j] * block scale,
+ * rounded to fp32 once per slot) * e4m3 value of yq[pos[t,j], h] ).  Errors
+ * as ep_combine, plus EP_ERR_UNSUPPORTED when H is not a multiple of the
+ * block width.
  */
 ep_status ep_combine_fp8(const void *yq, const void *yscales, int32_t scale_dtype, int32_t y_rows,
                          const int32_t *pos, const float *topk_w, int32_t T, int32_t H, int32_t k,
@@ -304,11 +304,13 @@ ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_row
  * Arguments as those calls (cfg as ep_gate; experts_per_rank and the layout
  * outputs as ep_get_layout; x, H, dtype, recv, recv_rows, recv_scales as
  * ep_dispatch).  1 <= T and T*k <= 4096 (larger batches use the separate
- * calls: EP_ERR_UNSUPPORTED).  workspace: >= 4 bytes of device memory,
- * 4-byte aligned, holding the grid barrier's counter (cleared by the call;
- * calls sharing it must not overlap on the GPU).  The grid barrier between
- * gating and layout waits at most about a second; if that ran out,
- * EP_FLAG_TIMEOUT is set in *err_flag and the outputs are incomplete.
+ * calls: EP_ERR_UNSUPPORTED).  workspace: >= 8 bytes of device memory,
+ * 4-byte aligned, holding the grid barrier's arrival count and generation:
+ * zero it once before the first call; each call leaves it ready for the
+ * next (calls sharing it must not overlap on the GPU).  The grid barrier
+ * between gating and layout waits at most about a second; if that ran out,
+ * EP_FLAG_TIMEOUT is set in *err_flag, the outputs are incomplete and the
+ * workspace must be zeroed again.
  * A device without cooperative launch returns EP_ERR_CUDA.
  */
 ep_status ep_decode_dispatch(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
@@ -324,11 +326,11 @@ ep_status ep_decode_dispatch(const float *scores, const float *bias, int32_t T, 
  * whose CTAs wait for missing_arrivals arrivals that never come (0: none
  * missing, the barrier completes).  With missing_arrivals > 0 every CTA
  * polls spin_limit times (1 <= spin_limit <= 2^24; each poll sleeps about
- * 64 ns plus a global load), then sets EP_FLAG_TIMEOUT in *err_flag and
+ * 32 ns plus a global load), then sets EP_FLAG_TIMEOUT in *err_flag and
  * returns -- the wait ends on its own and the context stays usable.
- * workspace as ep_decode_dispatch.  The pages have no counterpart to this
- * call; it exists so that the timeout path is tested on the GPU without a
- * hang.
+ * workspace: >= 8 bytes, 4-byte aligned, cleared by this call.  The pages
+ * have no counterpart to this call; it exists so that the timeout path is
+ * tested on the GPU without a hang.
  */
 ep_status ep_selftest_grid_barrier(int32_t missing_arrivals, int64_t spin_limit, int32_t *err_flag,
                                    void *workspace, size_t workspace_bytes, void *stream);

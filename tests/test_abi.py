@@ -164,7 +164,7 @@ def test_decode_entry_points_host_checks(lib):
     assert dd(128, H=7232) == 2                        # FP8 needs H % 128
     assert dd(128, dtype=7) == 1
     assert dd(128, ws=None) == 1
-    assert dd(128, wsb=2) == 1
+    assert dd(128, wsb=4) == 1
     assert dd(128, c=_cfg(ep, top_k=0)) == 1
     sb = lib.ep_selftest_grid_barrier
     assert sb(-1, 100, FAKE, FAKE, 64, None) == 1
