@@ -96,6 +96,62 @@ def recorded_traffic(op):
     return None if v is None else int(v)
 
 
+class Replicas:
+    """One process per GPU, each an independent replica of the path on its
+    own seeded batch: the tokens are data-parallel, so there is no collective
+    on the data path.  The only collectives are the barriers around the timed
+    region and the max over ranks of the measured times.  `value` is the
+    tokens of all ranks over that max time (weak scaling)."""
+
+    SEED_STRIDE = 1000
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self._dist = None
+        self._device = None
+
+    def init(self, backend, device):
+        """Join the process group (only when there is more than one rank)."""
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self._dist = dist
+        self._device = device
+        return self
+
+    def seed_offset(self):
+        return self.SEED_STRIDE * self.rank
+
+    def is_printer(self):
+        return self.rank == 0
+
+    def barrier(self):
+        if self._dist is not None:
+            self._dist.barrier()
+
+    def max(self, x):
+        """The maximum of a float over all ranks (x itself for one rank)."""
+        if self._dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self._device)
+        self._dist.all_reduce(t, op=self._dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def tokens_per_s(self, tokens_per_rank, ms):
+        return self.world * tokens_per_rank / (ms * 1e-3)
+
+    def close(self):
+        if self._dist is not None:
+            self._dist.destroy_process_group()
+            self._dist = None
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks / throttle reasons; only the samples
     taken between mark_start() and mark_end() (the timed region) count."""
@@ -221,20 +277,17 @@ class PathRunner:
 
 def run_ours(args):
     import torch
-    import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rep = Replicas()
+    world, local = rep.world, rep.local
     torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    rep.init("nccl", torch.device("cuda", local))
 
     from combine_group_limited_gb300 import build as epbuild
     epbuild.build()
 
     cfg = synth.config(WORKLOAD)
-    r = PathRunner(cfg, seed_offset=1000 * rank)
+    r = PathRunner(cfg, seed_offset=rep.seed_offset())
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     flush_rd = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda").fill_(1)
@@ -255,8 +308,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
+    rep.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
@@ -268,27 +320,19 @@ def run_ours(args):
                 ev[s][i + 1].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
-    if world > 1:
-        dist.barrier()
+    rep.barrier()
     if int(r.err.item()) != 0:
         raise RuntimeError("device error flag set: %d" % int(r.err.item()))
 
     per_op = {op: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)] for i, op in enumerate(ops)}
     step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
-    ms_per_step = sum(step_ms) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = rep.max(sum(step_ms) / args.steps)
 
     # end to end through the public API: pinned host inputs -> device -> path -> host output
     e2e = run_e2e(r, args)
-    if world > 1:
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms"] = float(t.item())
+    e2e["ms"] = rep.max(e2e["ms"])
 
-    if rank == 0:
+    if rep.is_printer():
         T = cfg["T"]
         peak, peak_kind = measured_hbm_peak()
         ab = algorithmic_bytes(cfg)
@@ -304,10 +348,10 @@ def run_ours(args):
                               "bytes": bytes_of[op], "kernel": kname[op]}
         dom = max(("dispatch", "combine"), key=lambda o: op_summary[o]["us"])
         traffic = recorded_traffic(kname[dom])
-        cpu = cpu_baseline(cfg, args) if world == 1 or rank == 0 else None
+        cpu = cpu_baseline(cfg, args)
         line = {
             "metric": METRIC,
-            "value": round(world * T / (ms_per_step * 1e-3), 1),
+            "value": round(rep.tokens_per_s(T, ms_per_step), 1),
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -330,7 +374,7 @@ def run_ours(args):
                          if peak_kind == "measured" else "fallback 6.8 TB/s", "unit": "GB/s",
                          "frac": op_summary[dom]["frac"], "traffic": traffic,
                          "algorithmic_bytes": bytes_of[dom]},
-            "e2e": {"value": round(world * T / (e2e["ms"] * 1e-3), 1), "unit": "tokens/s",
+            "e2e": {"value": round(rep.tokens_per_s(T, e2e["ms"]), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "ms_per_step": round(e2e["ms"], 4),
                     "method": "public API, pinned host buffers; H2D of scores then x in %d token chunks, "
@@ -340,8 +384,7 @@ def run_ours(args):
             "gpu_launches": PathRunner.LAUNCHES_PER_STEP * args.steps,
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    rep.close()
 
 
 def run_e2e(r, args, chunks=8):
@@ -448,8 +491,8 @@ def cpu_baseline(cfg, args, tokens=None, reps=3):
 
 def run_reference(args):
     """--impl reference: the CPU oracle, as it stands, on this workload."""
-    if int(os.environ.get("RANK", "0")) != 0:
-        return
+    if not Replicas().is_printer():
+        return                       # the other ranks exit 0 without work
     cfg = synth.config(WORKLOAD)
     per_token_s = 0.45e-3
     n_steps = args.steps + args.warmup
@@ -521,7 +564,39 @@ def run_sweep(args):
             torch.cuda.synchronize()
             if i >= 3:
                 ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+        # the event clock ticks in steps of about 2 us here: the mean over
+        # many repetitions (random phase) resolves below a tick, a median
+        # does not
+        return statistics.mean(ts)
+
+    def hot(fn, per_graph=20, replays=20):
+        """Back-to-back calls replayed from a CUDA graph, no flush between
+        them: the per-call device time of a latency-bound op with its
+        inputs L2-resident (as in a decode loop).  None if capture fails."""
+        try:
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(per_graph):
+                        fn()
+            stream.wait_stream(side)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(replays):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / (replays * per_graph)
+        except RuntimeError:
+            torch.cuda.synchronize()
+            return None
 
     names = args.configs.split(",") if args.configs else list(synth.CONFIGS)
     for name in names:
@@ -566,12 +641,17 @@ def run_sweep(args):
             us = timed(fn, args.reps)
             gbs = nb[op] / (us * 1e-6) / 1e9
             res[op] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb[op]}
+            if T * k <= 8192:                           # small enough to be latency-bound
+                h = hot(fn)
+                res[op]["hot_us"] = None if h is None else round(h, 3)
         dsp = "dispatch_fp8" if H % 128 == 0 else "dispatch_bf16"
         step = lambda: (r.gate(), r.layout(), ops[dsp](), r.combine())  # noqa: E731
         step_us = timed(step, args.reps)
         if "decode_fused" in ops:
             sep = lambda: (r.gate(), r.layout(), r.dispatch())  # noqa: E731
-            res["decode_separate"] = {"us": round(timed(sep, args.reps), 2)}
+            h = hot(sep)
+            res["decode_separate"] = {"us": round(timed(sep, args.reps), 2),
+                                      "hot_us": None if h is None else round(h, 3)}
         line = {"sweep": name, "T": T, "H": H, "E": E, "k": k, "peak_GBs": peak, "peak_source": peak_kind,
                 "step_us": round(step_us, 2), "step_tokens_per_s": round(T / (step_us * 1e-6), 1),
                 "step_dispatch": dsp, "ops": res}

@@ -74,7 +74,7 @@ def test_dispatch_full_size(ep, name, dtype):
     _dispatch_both(ep, inp["x"], _layout_pos(cfg, inp), dtype)
 
 
-@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (3, 24, 2), (17, 128, 3), (33, 384, 8), (9, 7168, 8), (130, 256, 5)])
+@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (3, 24, 2), (17, 128, 3), (33, 384, 8), (9, 7168, 8), (130, 256, 5), (5, 16384, 64)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_dispatch_small_shapes_with_empty_slots(ep, T, H, k, dtype):
     if dtype == "fp8" and H % 128:

@@ -45,7 +45,7 @@ def test_layout_full_size(ep, name):
 
 @pytest.mark.parametrize("T,k,E,epr", [
     (1, 1, 1, 1), (1, 8, 256, 8), (5, 3, 12, 4), (255, 8, 256, 8), (257, 8, 256, 8), (1000, 2, 8, 1),
-    (3000, 6, 1024, 32), (777, 16, 64, 64), (4097, 1, 16, 2),
+    (3000, 6, 1024, 32), (777, 16, 64, 64), (4097, 1, 16, 2), (300, 64, 1024, 16), (70, 64, 256, 8), (50, 64, 1024, 16),
 ])
 def test_layout_random_with_skips_and_duplicates(ep, T, k, E, epr):
     """Arbitrary index tensors: -1 slots, repeated experts in one token,
@@ -53,6 +53,14 @@ def test_layout_random_with_skips_and_duplicates(ep, T, k, E, epr):
     rng = np.random.default_rng(T * 31 + k)
     idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
     _check(ep, idx, E, epr)
+
+
+def test_layout_large_batch(ep):
+    """Two million entries (4096 tiles): the multi-tile scan at a size well
+    past any of the workloads, against the oracle."""
+    rng = np.random.default_rng(11)
+    idx = rng.integers(0, 256, size=(262144, 8)).astype(np.int32)
+    _check(ep, idx, 256, 8)
 
 
 def test_layout_every_token_on_the_same_experts(ep):
