@@ -528,7 +528,7 @@ def op_bytes(cfg):
     fp8_row = H + H // 32                          # e4m3 codes + scales (1x128 fp32 or 1x32 E8M0)
     b = algorithmic_bytes(cfg)
     return {
-        "gate": b["gate"], "layout": b["layout"], "layout_capacity": b["layout"],
+        "gate": b["gate"], "layout": b["layout"], "gate_layout": b["gate"] + b["layout"], "layout_capacity": b["layout"],
         "dispatch_bf16": b["dispatch_bf16"], "dispatch_fp8": b["dispatch_fp8"],
         "dispatch_mxfp8": T * (2 * H + k * fp8_row + 4 * k),
         "combine": b["combine"], "combine_fp8": T * (k * fp8_row + 8 * k + 2 * H),
@@ -615,6 +615,8 @@ def run_sweep(args):
         ops = {
             "gate": lambda: r.gate(),
             "layout": lambda: r.layout(),
+            "gate_layout": lambda: ep.ep_gate_layout(r.scores, r.bias, gc, epr, topk_idx=r.topk_idx, topk_w=r.topk_w,
+                                                     out=r.lay, workspace=ws),
             "layout_capacity": lambda: ep.ep_get_layout_capacity(r.topk_idx, E, epr, cap, workspace=ws),
             "dispatch_bf16": lambda: ep.ep_dispatch(r.x, r.lay.pos, "bf16", recv=recv_b),
             "dispatch_mxfp8": lambda: ep.ep_dispatch(r.x, r.lay.pos, "mxfp8", recv=recv_mq, recv_scales=recv_me),

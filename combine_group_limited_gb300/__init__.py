@@ -11,4 +11,5 @@ from ._binding import (  # noqa: F401
     EP_DTYPE_MXFP8_E4M3_B32, EP_FLAG_BAD_EXPERT, EP_FLAG_BAD_ROW, EP_FLAG_TIMEOUT, EP_OK, EP_SCORE_RAW, EP_SCORE_SOFTMAX, EXPORTS,
     CapLayout, EpError, GateCfg, Layout, alloc_layout, alloc_layout_workspace, ep_combine, ep_combine_backward,
     ep_combine_fp8, ep_decode_dispatch, ep_dispatch, ep_dispatch_backward, ep_gate, ep_get_layout, ep_get_layout_capacity,
-    ep_get_layout_noalloc, ep_layout_workspace_bytes, ep_selftest_grid_barrier, gate_cfg, load, status_str)
+    ep_gate_layout, ep_get_layout_noalloc, ep_layout_workspace_bytes, ep_selftest_grid_barrier, gate_cfg, load,
+    status_str)

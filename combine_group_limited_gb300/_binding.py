@@ -21,7 +21,8 @@ EP_SCORE_RAW, EP_SCORE_SOFTMAX = 0, 1
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128, EP_DTYPE_MXFP8_E4M3_B32 = 0, 1, 2
 
 # Symbols include/ep.h declares (checked by the CPU test suite).
-EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch",
+EXPORTS = ("ep_gate", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_noalloc", "ep_gate_layout",
+           "ep_dispatch",
            "ep_combine", "ep_combine_fp8", "ep_get_layout_capacity", "ep_dispatch_backward", "ep_combine_backward",
            "ep_decode_dispatch", "ep_selftest_grid_barrier", "ep_status_str")
 
@@ -56,6 +57,7 @@ def load():
     lib.ep_layout_workspace_bytes.restype = sz
     lib.ep_get_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]
     lib.ep_get_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+    lib.ep_gate_layout.argtypes = [P, P, i32, ctypes.POINTER(GateCfg), i32, P, P, P, P, P, P, P, P, P, P, P, sz, P]
     lib.ep_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, i32, P, P, P]
     lib.ep_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P]
     lib.ep_combine_fp8.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, P, P, P]
@@ -154,7 +156,7 @@ def alloc_layout_workspace(T, k, E, experts_per_rank, device="cuda"):
     n = ep_layout_workspace_bytes(T, k, E, experts_per_rank)
     if n == 0:
         raise ValueError("invalid layout sizes")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)  # ep_gate_layout wants its first 4 bytes zero
 
 
 def ep_get_layout(topk_idx, num_experts, experts_per_rank, out=None, workspace=None, err_flag=None, stream=None):
@@ -176,6 +178,40 @@ def ep_get_layout(topk_idx, num_experts, experts_per_rank, out=None, workspace=N
         _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.pos), _ptr(out.src), _ptr(err_flag),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def ep_gate_layout(scores, bias, cfg, experts_per_rank, topk_idx=None, topk_w=None, out=None, workspace=None,
+                   err_flag=None, stream=None):
+    """Steps 1 and 2 in one call (ep_gate, then ep_get_layout of its
+    experts; the same results).  The workspace's first 4 bytes must be zero
+    (alloc_layout_workspace gives such a buffer; calls leave them zero).
+    Returns (topk_idx, topk_w, Layout)."""
+    lib = load()
+    _dev(scores, torch.float32, "scores")
+    if scores.dim() != 2 or scores.shape[1] != cfg.num_experts:
+        raise ValueError("scores must be [T, num_experts]")
+    T, k, E, epr = scores.shape[0], cfg.top_k, cfg.num_experts, experts_per_rank
+    if bias is not None:
+        _dev(bias, torch.float32, "bias", (E,))
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=scores.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=scores.device)
+    _dev(topk_idx, torch.int32, "topk_idx", (T, k))
+    _dev(topk_w, torch.float32, "topk_w", (T, k))
+    if out is None:
+        if epr < 1 or E % epr:
+            raise ValueError("experts_per_rank must divide num_experts")
+        out = alloc_layout(T, k, E, epr, scores.device)
+    if workspace is None:
+        workspace = alloc_layout_workspace(T, k, E, epr, scores.device)
+    if err_flag is not None:
+        _dev(err_flag, torch.int32, "err_flag")
+    _check("ep_gate_layout", lib.ep_gate_layout(
+        _ptr(scores), _ptr(bias), T, ctypes.byref(cfg), epr, _ptr(topk_idx), _ptr(topk_w), _ptr(out.expert_count),
+        _ptr(out.expert_off), _ptr(out.rank_count), _ptr(out.rank_off), _ptr(out.rank_tokens), _ptr(out.pos),
+        _ptr(out.src), _ptr(err_flag), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, out
 
 
 def ep_get_layout_noalloc(topk_idx, num_experts, experts_per_rank, out, err_flag=None, stream=None):

@@ -19,6 +19,7 @@
 //      its share of the distinct-token counts;
 //   4. it scatters its own tokens' rows (dispatch_impl.cuh).
 // Results are the ones the separate calls give, bit for bit.
+#include "coop.cuh"
 #include "dispatch_impl.cuh"
 #include "gate_impl.cuh"
 
@@ -54,59 +55,6 @@ struct DecodeArgs {
     long long spin_limit;
 };
 
-// All CTAs of the (cooperative) grid arrive once; the wait is bounded.
-// word[0] counts arrivals, word[1] is a generation number: the last CTA to
-// arrive resets the count and advances the generation, which releases the
-// others -- so the barrier leaves its two words ready for the next launch
-// and needs no clearing between calls (only zeroing before the first).
-// Returns false, with EP_FLAG_TIMEOUT set, if the limit ran out (the words
-// are then left mid-barrier and must be zeroed again).
-__device__ bool grid_barrier(unsigned *word, unsigned expected, long long spin_limit, int32_t *err_flag)
-{
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned *count = word, *gen = word + 1;
-        unsigned g0;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(gen) : "memory");
-        __threadfence();  // this CTA's global writes before its arrival
-        const unsigned arrived = atomicAdd(count, 1u) + 1u;
-        bool ok = true;
-        if (arrived == expected) {
-            // release the others first; the count only has to be back at
-            // zero before the next launch, which starts after this one ends
-            atomicAdd(gen, 1u);
-            atomicExch(count, 0u);
-        } else {
-            unsigned g = g0;
-            long long it = 0;
-            for (;;) {
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(gen) : "memory");
-                if (g != g0 || ++it >= spin_limit)
-                    break;
-                __nanosleep(32);
-            }
-            ok = g != g0;
-        }
-        s_ok = ok;
-        if (!ok && err_flag)
-            atomicOr(err_flag, 4);
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
-__device__ __forceinline__ int warp_incl_scan(int v, int lane)
-{
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(kFullMask, v, off);
-        if (lane >= off)
-            v += n;
-    }
-    return v;
-}
-
 template <int EPL>
 __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeArgs a)
 {
@@ -121,8 +69,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
 
     // 1. gating of this CTA's tokens
     for (int t = t_lo + warp; t < t_hi; t += kDecWarps)
-        gate_token<EPL>(a.scores, a.bias, t, a.gp, a.group_lanes, a.vec_rows, reinterpret_cast<float *>(dsm) + warp * E,
-                        a.topk_idx, a.topk_w);
+        gate_token<EPL>(a.scores, a.bias, t, a.gp, a.group_lanes, a.vec_rows,
+                        reinterpret_cast<uint32_t *>(dsm) + warp * gate_warp_words<EPL>(), a.topk_idx, a.topk_w);
     if (blockIdx.x == 0)
         for (int r = threadIdx.x; r < R; r += blockDim.x)
             a.rank_tokens[r] = 0;  // accumulated by every CTA after the barrier
@@ -339,7 +287,6 @@ cudaError_t launch_epl(DecodeArgs a, cudaStream_t st)
 
 }  // namespace
 
-constexpr long long kDecodeSpinLimit = 1LL << 21;  // about a second of polling
 
 size_t decode_max_entries() { return kMaxEntries; }
 
@@ -373,7 +320,7 @@ cudaError_t launch_decode(const float *scores, const float *bias, int T, const G
     a.err_flag = err_flag;
     a.barrier = static_cast<unsigned *>(barrier_word);
     a.barrier_extra = 0;
-    a.spin_limit = kDecodeSpinLimit;
+    a.spin_limit = kGridSpinLimit;
     if (gp.E <= 32)
         return launch_epl<1>(a, st);
     if (gp.E <= 64)

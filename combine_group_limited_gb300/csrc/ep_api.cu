@@ -154,6 +154,48 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
                                       static_cast<cudaStream_t>(stream)));
 }
 
+ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
+                         int32_t experts_per_rank, int32_t *topk_idx, float *topk_w, int32_t *expert_count,
+                         int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (T < 0)
+        return EP_ERR_INVALID_ARG;
+    const ep_status c = check_gate_cfg(cfg);
+    if (c != EP_OK)
+        return c;
+    const int E = cfg->num_experts, k = cfg->top_k;
+    const ep_status l = check_layout_args(T, k, E, experts_per_rank);
+    if (l != EP_OK)
+        return l;
+    if (!expert_count || !expert_off || !rank_count || !rank_off || !rank_tokens || !workspace)
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!scores || !topk_idx || !topk_w || !pos || !src))
+        return EP_ERR_INVALID_ARG;
+    if (workspace_bytes < ep::layout_workspace_bytes(T, k, E, experts_per_rank))
+        return EP_ERR_INVALID_ARG;
+    const void *p4[] = {scores, bias, topk_idx, topk_w, expert_count, expert_off, rank_count, rank_off, rank_tokens,
+                        pos,    src,  err_flag};
+    for (const void *q : p4)
+        if (q && !aligned(q, 4))
+            return EP_ERR_ALIGNMENT;
+    if (!aligned(workspace, 16))
+        return EP_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ep::GateParams gp = gate_params(cfg);
+    if (T > 0 && ep::route_supported(T, k, E))
+        return launched(ep::launch_route(scores, bias, &gp, nullptr, topk_idx, topk_w, T, k, E, experts_per_rank,
+                                         expert_count, expert_off, rank_count, rank_off, rank_tokens, pos, src,
+                                         err_flag, workspace, st));
+    // batches the single launch does not cover: the two steps' own kernels
+    cudaError_t e = ep::launch_gate(scores, bias, T, gp, topk_idx, topk_w, st);
+    if (e == cudaSuccess)
+        e = ep::launch_layout(topk_idx, T, k, E, experts_per_rank, expert_count, expert_off, rank_count, rank_off,
+                              rank_tokens, pos, src, err_flag, workspace, st);
+    return launched(e);
+}
+
 ep_status ep_dispatch(const void *x, int32_t T, int32_t H, int32_t k, const int32_t *pos, int32_t dtype, void *recv,
                       int32_t recv_rows, void *recv_scales, int32_t *err_flag, void *stream)
 {

@@ -11,16 +11,15 @@
 //
 // Layout: lane l of the token's warp owns the EPL contiguous experts
 // [l*EPL, (l+1)*EPL), loaded as 16-byte vectors when the row allows.  Each
-// lane turns its keys into order-preserving uint32s packed with the local
-// index (larger key first, then lower index) and sorts them once with a
-// bitonic network.  When a group is a power-of-two run of whole lanes
-// (E=256, G=8: 4 lanes of 8), the group's largest keys come from the lanes'
-// sorted heads merged by xor shuffles in the integer domain; otherwise lane g
-// scans group g in shared memory.  Each top-k round is then a warp max over
-// the lanes' heads (redux.sync) and a warp min over the expert indices that
-// reach it, so ties resolve to the lower index without 64-bit shuffles; the
-// winning lane shifts its list.  The unbiased score of each chosen expert is
-// re-read from the (cached) score row at the end.
+// lane sorts its order-preserving uint32 keys once (a bitonic network of
+// max/min pairs).  When a group is a power-of-two run of whole lanes (E=256,
+// G=8: 4 lanes of 8), the group's largest keys come from the lanes' sorted
+// heads merged by xor shuffles; otherwise lane g scans group g in shared
+// memory.  Each top-k round is one warp max over the lanes' heads; the
+// lowest lane holding it wins (lower lanes own lower indices) and steps to
+// its next key.  Only at the end does a lane find which of its experts its
+// won keys were (equal keys lowest index first).  The unbiased score of each
+// chosen expert is re-read from the (cached) score row.
 #include "gate_impl.cuh"
 
 namespace ep {
@@ -37,12 +36,13 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const float *__restr
                                                             int32_t *__restrict__ topk_idx,
                                                             float *__restrict__ topk_w)
 {
-    extern __shared__ float gate_smem[];  // only for groups that are not whole-lane runs
+    extern __shared__ uint32_t gate_smem[];  // gate_warp_words<EPL>() per warp
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kGateWarps + warp;
     if (t >= T)
         return;  // the whole warp leaves together
-    gate_token<EPL>(scores, bias, t, p, group_lanes, vec_rows, gate_smem + warp * p.E, topk_idx, topk_w);
+    gate_token<EPL>(scores, bias, t, p, group_lanes, vec_rows, gate_smem + warp * gate_warp_words<EPL>(), topk_idx,
+                    topk_w);
 }
 
 template <int EPL>

@@ -41,9 +41,10 @@ __device__ __forceinline__ float key_value(uint32_t o)
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// Descending bitonic sort of N (a power of two) packed candidates.
+// Descending bitonic sort of N (a power of two) keys; each compare-exchange
+// is one max and one min.
 template <int N>
-__device__ __forceinline__ void sort_desc(unsigned long long (&a)[N])
+__device__ __forceinline__ void sort_desc(uint32_t (&a)[N])
 {
 #pragma unroll
     for (int size = 2; size <= N; size <<= 1) {
@@ -53,32 +54,43 @@ __device__ __forceinline__ void sort_desc(unsigned long long (&a)[N])
             for (int i = 0; i < N; ++i) {
                 const int j = i ^ stride;
                 if (j > i) {
+                    const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
                     const bool desc = (i & size) == 0;
-                    const unsigned long long x = a[i], y = a[j];
-                    if (desc ? (x < y) : (x > y)) {
-                        a[i] = y;
-                        a[j] = x;
-                    }
+                    a[i] = desc ? hi : lo;
+                    a[j] = desc ? lo : hi;
                 }
             }
         }
     }
 }
 
-// Candidate = key in the high word, (EPL-1-i) in the low word: the larger
-// key wins, then the lower index.  0 marks "no candidate".
+// Words of per-warp shared scratch gate_token needs: every lane's sorted
+// keys, then the chosen experts of the k slots.  (The general group path
+// also stages the row's keys there first: E <= 32 * EPL words.)
 template <int EPL>
-__device__ __forceinline__ unsigned long long pack_cand(uint32_t ord, int i)
+__host__ __device__ constexpr int gate_warp_words()
 {
-    return ord ? ((unsigned long long)ord << 32) | (unsigned)(EPL - 1 - i) : 0ull;
+    return 32 * EPL + 32;
 }
 
-// Gates token t with the calling warp (all 32 lanes).  warp_smem: E floats
-// of shared memory for this warp, used only when group_lanes == 0 and the
-// groups are limited.  Lane j < k writes slot j.
+// Gates token t with the calling warp (all 32 lanes).  wsm: the warp's
+// gate_warp_words<EPL>() words of shared memory.  Lane j < k writes slot j.
+//
+// Lane l owns experts [l*EPL, (l+1)*EPL).  It maps its keys to
+// order-preserving uint32s (0 = no candidate) and sorts a copy descending.
+// Group scores: for groups that are power-of-two runs of whole lanes, the
+// largest keys of a group are among its lanes' sorted heads (merged with xor
+// shuffles); other groups are scanned by one lane each from shared memory.
+// Each top-k round is a warp max over the lanes' current heads; among lanes
+// holding that key the lowest lane wins (its experts have the lower
+// indices), and it advances to its next sorted key (read from shared
+// memory).  A lane's wins took its sorted keys in order, so at the end it
+// finds each won key among its unsorted keys -- equal keys go lowest index
+// first, the order the tie rule asks for -- and writes the expert of that
+// round's slot.
 template <int EPL>
 __device__ __forceinline__ void gate_token(const float *__restrict__ scores, const float *__restrict__ bias, int t,
-                                           const GateParams &p, int group_lanes, int vec_rows, float *warp_smem,
+                                           const GateParams &p, int group_lanes, int vec_rows, uint32_t *wsm,
                                            int32_t *__restrict__ topk_idx, float *__restrict__ topk_w)
 {
     const int lane = threadIdx.x & 31;
@@ -118,12 +130,13 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
     for (int i = 0; i < EPL; ++i)
         ord[i] = (e0 + i < E) ? ordered_key(key[i]) : 0u;
 
-    unsigned long long cand[EPL];
+    uint32_t srt[EPL];
+    bool lane_kept = true;
     const bool grouped = p.Kg < p.G;
     if (grouped && group_lanes == 0) {
         // General groups: lane g scans group g's keys in shared memory.
         const int gsize = E / p.G;
-        float *skey = warp_smem;
+        float *skey = reinterpret_cast<float *>(wsm);
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if (e0 + i < E)
@@ -156,38 +169,54 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
         for (int i = 0; i < EPL; ++i)
             if (e0 + i < E && !((kept >> ((e0 + i) / gsize)) & 1u))
                 ord[i] = 0u;
+        __syncwarp();  // the staged keys are dead; wsm now holds the lists
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            cand[i] = pack_cand<EPL>(ord[i], i);
-        sort_desc(cand);
+            srt[i] = ord[i];
+        sort_desc(srt);
     } else {
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            cand[i] = pack_cand<EPL>(ord[i], i);
-        sort_desc(cand);
+            srt[i] = ord[i];
+        sort_desc(srt);
         if (grouped) {
             // Groups are runs of group_lanes whole lanes (a power of two): the
             // group's largest keys are among its lanes' sorted heads.
-            uint32_t top[kMaxKin];
-#pragma unroll
-            for (int q = 0; q < kMaxKin; ++q)
-                top[q] = (q < EPL) ? (uint32_t)(cand[q < EPL ? q : 0] >> 32) : 0u;
-            for (int off = 1; off < group_lanes; off <<= 1) {
-                uint32_t other[kMaxKin];
+            float gs;
+            if (p.kin <= 2) {
+                uint32_t a0 = srt[0], a1 = EPL > 1 ? srt[EPL > 1 ? 1 : 0] : 0u;
+                for (int off = 1; off < group_lanes; off <<= 1) {
+                    const uint32_t b0 = __shfl_xor_sync(kFullMask, a0, off);
+                    const uint32_t b1 = __shfl_xor_sync(kFullMask, a1, off);
+                    const uint32_t n1 = max(min(a0, b0), max(a1, b1));
+                    a0 = max(a0, b0);
+                    a1 = n1;
+                }
+                gs = key_value(a0);
+                if (p.kin == 2)
+                    gs = gs + key_value(a1);
+            } else {
+                uint32_t top[kMaxKin];
 #pragma unroll
                 for (int q = 0; q < kMaxKin; ++q)
-                    other[q] = __shfl_xor_sync(kFullMask, top[q], off);
+                    top[q] = (q < EPL) ? srt[q < EPL ? q : 0] : 0u;
+                for (int off = 1; off < group_lanes; off <<= 1) {
+                    uint32_t other[kMaxKin];
 #pragma unroll
-                for (int q = 0; q < kMaxKin; ++q)
-                    offer_u(top, other[q]);
+                    for (int q = 0; q < kMaxKin; ++q)
+                        other[q] = __shfl_xor_sync(kFullMask, top[q], off);
+#pragma unroll
+                    for (int q = 0; q < kMaxKin; ++q)
+                        offer_u(top, other[q]);
+                }
+                gs = key_value(top[0]);
+#pragma unroll
+                for (int q = 1; q < kMaxKin; ++q)
+                    if (q < p.kin)
+                        gs = gs + key_value(top[q]);
             }
             const int my_group = lane / group_lanes;
             const bool leader = (lane % group_lanes) == 0 && my_group < p.G;
-            float gs = key_value(top[0]);
-#pragma unroll
-            for (int q = 1; q < kMaxKin; ++q)
-                if (q < p.kin)
-                    gs = gs + key_value(top[q]);
             uint32_t kept = 0u;
             for (int r = 0; r < p.Kg; ++r) {
                 const bool c = leader && !((kept >> my_group) & 1u);
@@ -198,36 +227,67 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
                 if (g < 32u)
                     kept |= 1u << g;
             }
-            if (!((kept >> my_group) & 1u)) {
-#pragma unroll
-                for (int i = 0; i < EPL; ++i)
-                    cand[i] = 0ull;
-            }
+            lane_kept = (kept >> my_group) & 1u;
         }
     }
 
-    // Top-k rounds over the lanes' sorted heads.
-    int my_e = 0;
-    for (int j = 0; j < p.k; ++j) {
-        const uint32_t hk = (uint32_t)(cand[0] >> 32);
-        const uint32_t mx = __reduce_max_sync(kFullMask, hk);
-        const uint32_t mine = (hk == mx && hk != 0u) ? (uint32_t)(e0 + EPL - 1 - (int)(cand[0] & 0xFFFFFFFFull))
-                                                     : 0xFFFFFFFFu;
-        const uint32_t wu = __reduce_min_sync(kFullMask, mine);
-        if (wu == mine && wu != 0xFFFFFFFFu) {
+    // This lane's sorted keys, for the rounds to read past the head.
+    uint32_t *lst = wsm + lane * EPL;
+    int32_t *s_e = reinterpret_cast<int32_t *>(wsm + 32 * EPL);
+    if (EPL % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i + 1 < EPL; ++i)
-                cand[i] = cand[i + 1];
-            cand[EPL - 1] = 0ull;
-        }
-        // Always a valid expert for finite scores; clamped so that even
-        // unsupported (NaN) input cannot index outside the score row.
-        if (lane == j)
-            my_e = wu < (uint32_t)E ? (int)wu : 0;
+        for (int i = 0; i < EPL; i += 4)
+            *reinterpret_cast<uint4 *>(lst + i) = make_uint4(srt[i], srt[i + 1], srt[i + 2], srt[i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            lst[i] = srt[i];
     }
+    s_e[lane] = 0;  // a slot no round fills (impossible for finite scores) stays in range
+    __syncwarp();
+
+    // Top-k rounds over the lanes' heads.
+    const int k = p.k;
+    uint32_t hk = lane_kept ? srt[0] : 0u;
+    int h = 0;
+    uint32_t won = 0u;  // bit j: this lane won round j
+    for (int j = 0; j < k; ++j) {
+        const uint32_t mx = __reduce_max_sync(kFullMask, hk);
+        const unsigned bal = __ballot_sync(kFullMask, hk == mx && mx != 0u);
+        if (bal != 0u && lane == __ffs(bal) - 1) {
+            won |= 1u << j;
+            ++h;
+            hk = h < EPL ? lst[h] : 0u;
+        }
+    }
+    // Experts of the won rounds: the n-th win took sorted key n; the lowest
+    // unused index holding that key is its expert.
+    uint32_t used = 0u;
+    int n = 0;
+    while (__any_sync(kFullMask, won != 0u)) {
+        if (won != 0u) {
+            const int j = __ffs(won) - 1;
+            won &= won - 1u;
+            const uint32_t kv = lst[n++];
+            uint32_t m = 0u;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                m |= (ord[i] == kv ? 1u : 0u) << i;
+            m &= ~used;
+            const int i = __ffs(m) - 1;
+            used |= 1u << i;
+            s_e[j] = e0 + i;
+        }
+    }
+    __syncwarp();
+    int my_e = 0;
+    if (lane < k) {
+        const int e = s_e[lane];
+        my_e = (unsigned)e < (unsigned)E ? e : 0;
+    }
+    __syncwarp();  // the scratch may be reused by the warp's next token
 
     // Weights from the unbiased score, sums taken in slot order.
-    const int k = p.k;
     const float my_s = (lane < k) ? __ldg(row + my_e) : 0.0f;
     float w;
     if (p.score_fn == 0) {
@@ -281,8 +341,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
 
 // Host-side launch plan shared by the gating launchers: whether groups are
 // power-of-two runs of whole lanes (group_lanes > 0), whether 16-byte row
-// loads are allowed, and the shared memory (floats per warp) the general
-// group path needs.
+// loads are allowed, and the shared memory words per warp gate_token needs.
 template <int EPL>
 inline void gate_plan(const GateParams &p, const float *scores, const float *bias, int &group_lanes, int &vec_rows,
                       int &warp_floats)
@@ -300,7 +359,7 @@ inline void gate_plan(const GateParams &p, const float *scores, const float *bia
                 (reinterpret_cast<uintptr_t>(bias) & 15) == 0)
                    ? 1
                    : 0;
-    warp_floats = (p.Kg < p.G && group_lanes == 0) ? p.E : 0;
+    warp_floats = gate_warp_words<EPL>();
 }
 
 }  // namespace ep

@@ -7,8 +7,11 @@
 // distinct experts fills at most T*k rows, so nothing here is read back to
 // the host.
 //
-// Batches of up to 4096 entries take one launch (layout_small_kernel); larger
-// ones take three launches over tiles of whole tokens (about 512 entries each):
+// Batches of up to 4096 entries take one launch (layout_small_kernel).  Larger
+// ones take one cooperative launch (route.cu) while a grid of one CTA per SM
+// covers them with at most 4096 entries per CTA; beyond that (and in
+// capacity mode) they take three launches over tiles of whole tokens (about
+// 512 entries each):
 //  1. count:  per tile, per-expert entry counts and per-rank distinct-token
 //             counts (shared-memory integer atomics; the totals do not depend
 //             on their order).  Workspace columns [E][tiles], [R][tiles].
@@ -562,12 +565,18 @@ int layout_num_tiles(int T, int k)
     return (T + tt - 1) / tt;
 }
 
+// Workspace: 256 bytes whose first 8 are the single-launch path's grid
+// barrier words (arrival count, generation; no other path touches them), then
+// either the per-tile
+// counts of the three-launch path or the per-CTA rows of the single-launch
+// one.
 size_t layout_workspace_bytes(int T, int k, int E, int epr)
 {
     const size_t nt = (size_t)layout_num_tiles(T, k);
     const size_t R = (size_t)(E / epr);
-    const size_t bytes = nt * ((size_t)E + R) * sizeof(int32_t);
-    return ((bytes + 255) / 256) * 256 + 256;
+    const size_t bytes = ((nt * ((size_t)E + R) * sizeof(int32_t) + 255) / 256) * 256 + 256;
+    const size_t single = route_workspace_bytes(E);
+    return bytes > single ? bytes : single;
 }
 
 cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int epr, int cap,
@@ -606,7 +615,15 @@ cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int
                                                             rank_count, rank_off, rank_tokens, pos, src, err_flag);
         return cudaGetLastError();
     }
-    int32_t *ws_cnt = static_cast<int32_t *>(workspace);
+    if (!capped && route_supported(T, k, E)) {
+        // one cooperative launch; its barrier's arrival count starts at zero
+        cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(unsigned), st);
+        if (e != cudaSuccess)
+            return e;
+        return launch_route(nullptr, nullptr, nullptr, topk_idx, nullptr, nullptr, T, k, E, epr, expert_count,
+                            expert_off, rank_count, rank_off, rank_tokens, pos, src, err_flag, workspace, st);
+    }
+    int32_t *ws_cnt = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + 256);
     int32_t *ws_rt = ws_cnt + (size_t)nt * E;
     layout_count_kernel<<<nt, kLayoutThreads, (E + R + kTileEntries) * sizeof(int32_t), st>>>(
         topk_idx, T, k, E, epr, tile_tok, nt, ws_cnt, ws_rt, err_flag);

@@ -37,8 +37,8 @@
  *    skipped and a bit is OR-ed into *err_flag (a device int32, may be NULL):
  *      EP_FLAG_BAD_EXPERT  an expert index neither -1 nor in [0, E)
  *      EP_FLAG_BAD_ROW     a receive row outside the buffer's rows
- *      EP_FLAG_TIMEOUT     a bounded device-side wait ran out (the fused
- *                          decode path's grid barrier); that work stopped
+ *      EP_FLAG_TIMEOUT     a bounded device-side wait ran out (the grid
+ *                          barrier of a cooperative launch); that work stopped
  *  - bf16 tensors are raw 16-bit bfloat16 patterns, row-major.
  *  - T*k rows always suffice for a receive buffer (top-k picks k distinct
  *    experts per token), so buffers are sized without reading any count
@@ -137,9 +137,14 @@ size_t ep_layout_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t expert
  * err_flag      device int32 or NULL: EP_FLAG_BAD_EXPERT is OR-ed in when an
  *               index is neither -1 nor in [0, E); that entry is skipped.
  * workspace     device scratch of at least ep_layout_workspace_bytes(...)
- *               bytes, 16-byte aligned; contents need no initialisation and
- *               are garbage afterwards.  It must not be shared by layouts
- *               in flight at the same time.
+ *               bytes, 16-byte aligned; contents need no initialisation.
+ *               Afterwards its first 4 bytes are zero (this call clears
+ *               them when it uses them) and the rest is garbage.  It must not be
+ *               shared by layouts in flight at the same time.
+ * Batches of more than 4096 entries run as one cooperative launch while a
+ * grid of one CTA per SM covers them with at most 4096 entries per CTA (a
+ * bounded grid barrier; if its wait runs out EP_FLAG_TIMEOUT is OR-ed into
+ * *err_flag and the outputs are incomplete), else as three launches.
  * Limits: 1 <= E <= 1024, experts_per_rank divides E, 1 <= k <= 64, T >= 0,
  * T*k < 2^31.  Errors: EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED,
  * EP_ERR_ALIGNMENT, EP_ERR_CUDA.
@@ -149,6 +154,37 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
                         int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace,
                         size_t workspace_bytes, void *stream);
+
+/*
+ * Steps 1 and 2 in one call: ep_gate, then ep_get_layout of the experts it
+ * chose, with the outputs of those two calls bit for bit ("DeepEP de DeepSeek
+ * ...", section "Group-limited gating algorithm"; "Expert Parallelism ...",
+ * section "Le principe de base").  Each is short and latency-bound at full
+ * batch size; here, while a grid of one CTA per SM covers the batch with at
+ * most 4096 entries per CTA, both run in one cooperative launch whose CTAs
+ * gate and count their own tokens, meet at one grid barrier and then place
+ * them.  Larger batches run the two calls' own kernels.
+ *
+ * Arguments: those of ep_gate (scores, bias, T, cfg, topk_idx, topk_w) and
+ * of ep_get_layout (experts_per_rank, expert_count .. src, err_flag), with
+ * the same layouts, limits and errors, except:
+ * workspace     at least ep_layout_workspace_bytes(T, cfg->top_k,
+ *               cfg->num_experts, experts_per_rank) bytes, 16-byte aligned,
+ *               whose first 4 bytes (the grid barrier's arrival count) are
+ *               zero before the call; the next 4 (its generation number)
+ *               may hold anything.  Every call that completes leaves the
+ *               count zero (so do ep_get_layout and ep_get_layout_capacity
+ *               on the same workspace): clear it once when the workspace is
+ *               allocated.  If the barrier's bounded wait runs out,
+ *               EP_FLAG_TIMEOUT is OR-ed into *err_flag, the outputs are
+ *               incomplete and the count must be cleared again.  Calls in
+ *               flight at the same time need separate workspaces.
+ */
+ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, const ep_gate_cfg *cfg,
+                         int32_t experts_per_rank, int32_t *topk_idx, float *topk_w, int32_t *expert_count,
+                         int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
+                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /*
  * ep_get_layout without a workspace argument, for callers that cannot

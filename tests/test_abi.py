@@ -172,3 +172,20 @@ def test_decode_entry_points_host_checks(lib):
     assert sb(1, (1 << 24) + 1, FAKE, FAKE, 64, None) == 1
     assert sb(1, 100, None, FAKE, 64, None) == 1
     assert sb(1, 100, ODD, ctypes.c_void_p(0x10001), 64, None) == 3
+
+
+def test_gate_layout_host_checks(lib):
+    import combine_group_limited_gb300 as ep
+    cfg = _cfg(ep)
+    n = lib.ep_layout_workspace_bytes(8192, 8, 256, 8)
+    gl = lambda T=8192, epr=8, c=cfg, ws=FAKE, wsb=n, s=FAKE: lib.ep_gate_layout(  # noqa: E731
+        s, None, T, ctypes.byref(c), epr, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, ws, wsb, None)
+    assert gl(T=-1) == 1
+    assert gl(epr=7) == 1
+    assert gl(c=_cfg(ep, top_k=0)) == 1
+    assert gl(c=_cfg(ep, num_experts=1024, n_groups=8)) == 2
+    assert gl(wsb=n - 1) == 1
+    assert gl(ws=None) == 1
+    assert gl(s=None) == 1
+    assert gl(ws=ctypes.c_void_p(0x10008)) == 3
+    assert gl(s=ctypes.c_void_p(0x10002)) == 3
