@@ -2,9 +2,10 @@
 
 One step = one pass of the whole path over one batch of the DeepSeek-V3-shaped
 workload (8192 tokens, hidden 7168, 256 experts in 8 groups, top-4 groups then
-top-8 experts, 32 logical ranks x 8 experts): group-limited gating -> layout
--> FP8 e4m3 1x128 dispatch -> weighted BF16 combine of the expert outputs
-(identity experts: the BF16-dispatched rows, made once before timing).
+top-8 experts, 32 logical ranks x 8 experts): group-limited gating and layout
+(one call, ep_gate_layout) -> FP8 e4m3 1x128 dispatch -> weighted BF16
+combine of the expert outputs (identity experts: the BF16-dispatched rows,
+made once before timing).
 
 Prints ONE JSON line (rank 0): whole-job tokens/s, per-op times and HBM
 GB/s, the roofline of the dominant kernel, an end-to-end figure through the
@@ -250,8 +251,9 @@ class PathRunner:
         self.y = ep.ep_dispatch(self.x, self.lay.pos, "bf16")
         torch.cuda.synchronize()
 
-    # the four launches of a step (gpu_launches counts them: 1 + 3 + 1 + 1)
-    LAUNCHES_PER_STEP = 6
+    # the launches of a step (gpu_launches counts them): gating and layout in
+    # one cooperative launch, then dispatch, then combine
+    LAUNCHES_PER_STEP = 3
 
     def gate(self):
         self.ep.ep_gate(self.scores, self.bias, self.gcfg, self.topk_idx, self.topk_w)
@@ -261,6 +263,12 @@ class PathRunner:
         self.ep.ep_get_layout(self.topk_idx, c["E"], c["experts_per_rank"], out=self.lay, workspace=self.ws,
                               err_flag=self.err)
 
+    def route(self):
+        """Gating and layout in one call (one cooperative launch)."""
+        c = self.cfg
+        self.ep.ep_gate_layout(self.scores, self.bias, self.gcfg, c["experts_per_rank"], topk_idx=self.topk_idx,
+                               topk_w=self.topk_w, out=self.lay, workspace=self.ws, err_flag=self.err)
+
     def dispatch(self):
         self.ep.ep_dispatch(self.x, self.lay.pos, "fp8", recv=self.recv_q, recv_scales=self.recv_s,
                             err_flag=self.err)
@@ -269,8 +277,7 @@ class PathRunner:
         self.ep.ep_combine(self.y, self.lay.pos, self.topk_w, out=self.out, err_flag=self.err)
 
     def step(self):
-        self.gate()
-        self.layout()
+        self.route()
         self.dispatch()
         self.combine()
 
@@ -290,7 +297,7 @@ def run_ours(args):
     r = PathRunner(cfg, seed_offset=rep.seed_offset())
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush_rd = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda").fill_(1)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")  # summed in fp32: no cast kernel
 
     def flush_l2(s):
         # Evict the step's data from L2: write a buffer twice the L2 size,
@@ -300,7 +307,7 @@ def run_ours(args):
         flush.fill_(s & 0xFF)
         flush_rd.sum()
 
-    ops = ("gate", "layout", "dispatch", "combine")
+    ops = ("route", "dispatch", "combine")
 
     for w in range(args.warmup):
         flush_l2(w)
@@ -336,10 +343,8 @@ def run_ours(args):
         T = cfg["T"]
         peak, peak_kind = measured_hbm_peak()
         ab = algorithmic_bytes(cfg)
-        bytes_of = {"gate": ab["gate"], "layout": ab["layout"], "dispatch": ab["dispatch_fp8"],
-                    "combine": ab["combine"]}
-        kname = {"gate": "gate_kernel", "layout": "layout_*_kernel", "dispatch": "dispatch_fp8_kernel",
-                 "combine": "combine_kernel"}
+        bytes_of = {"route": ab["gate"] + ab["layout"], "dispatch": ab["dispatch_fp8"], "combine": ab["combine"]}
+        kname = {"route": "route_kernel", "dispatch": "dispatch_fp8_kernel", "combine": "combine_kernel"}
         op_summary = {}
         for op in ops:
             us = 1e3 * statistics.mean(per_op[op])
@@ -426,8 +431,7 @@ def run_e2e(r, args, chunks=8):
                 ev.record(s_in)
                 ev_x.append(ev)
         comp.wait_event(ev_scores)
-        r.gate()
-        r.layout()
+        r.route()
         for i in range(chunks):
             a, b = bounds[i], bounds[i + 1]
             comp.wait_event(ev_x[i])
@@ -549,7 +553,7 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     peak, peak_kind = measured_hbm_peak()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush_rd = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda").fill_(1)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")  # summed in fp32: no cast kernel
     stream = torch.cuda.current_stream()
 
     def timed(fn, reps):
@@ -647,7 +651,7 @@ def run_sweep(args):
                 h = hot(fn)
                 res[op]["hot_us"] = None if h is None else round(h, 3)
         dsp = "dispatch_fp8" if H % 128 == 0 else "dispatch_bf16"
-        step = lambda: (r.gate(), r.layout(), ops[dsp](), r.combine())  # noqa: E731
+        step = lambda: (r.route(), ops[dsp](), r.combine())  # noqa: E731
         step_us = timed(step, args.reps)
         if "decode_fused" in ops:
             sep = lambda: (r.gate(), r.layout(), r.dispatch())  # noqa: E731
