@@ -20,6 +20,9 @@
 // bf16 of the exact product (for products in the normal fp32 range).  The
 // dots are reduced in a fixed order (each thread's chunks in sequence, a warp
 // xor-tree, then the warps in order), so grad_w does not depend on timing.
+// As in the combine, the next token's rows and weights are fetched while
+// one is processed, and the block size spreads a row evenly over the warps
+// (the reduction order then depends on H, never on timing).
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -47,7 +50,7 @@ __device__ __forceinline__ float exact_product_for_bf16(float w, float g)
     return p;
 }
 
-__global__ void __launch_bounds__(kBwdThreads) combine_backward_kernel(
+__global__ void __launch_bounds__(kBwdThreads, 3) combine_backward_kernel(
     const uint16_t *__restrict__ grad_out, const uint16_t *__restrict__ y, const int32_t *__restrict__ pos,
     const float *__restrict__ w, int T, int H, int k, uint16_t *__restrict__ grad_y, float *__restrict__ grad_w,
     long long rows, int32_t *__restrict__ err_flag)
@@ -55,28 +58,40 @@ __global__ void __launch_bounds__(kBwdThreads) combine_backward_kernel(
     __shared__ int32_t s_pos[kMaxK];
     __shared__ float s_w[kMaxK];
     __shared__ float s_part[kSlotBatch][kBwdWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int C = H / 8;
+    const bool loader = threadIdx.x < k;
+    int np = -1;
+    float nw = 0.0f;
+    if (loader && blockIdx.x < T) {
+        np = __ldg(pos + (size_t)blockIdx.x * k + threadIdx.x);
+        nw = __ldg(w + (size_t)blockIdx.x * k + threadIdx.x);
+    }
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
-        if (threadIdx.x < k) {
-            int p = __ldg(pos + (size_t)t * k + threadIdx.x);
+        if (loader) {
+            int p = np;
             if (p >= rows) {
                 if (err_flag)
                     atomicOr(err_flag, 2);
                 p = -1;
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+            s_w[threadIdx.x] = nw;
         }
         __syncthreads();
+        const int tn = t + gridDim.x;  // prefetch the next token's rows and weights
+        if (loader && tn < T) {
+            np = __ldg(pos + (size_t)tn * k + threadIdx.x);
+            nw = __ldg(w + (size_t)tn * k + threadIdx.x);
+        }
         const uint16_t *grow = grad_out + (size_t)t * H;
         for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
             float dot[kSlotBatch];
 #pragma unroll
             for (int u = 0; u < kSlotBatch; ++u)
                 dot[u] = 0.0f;
-            for (int c = threadIdx.x; c < C; c += kBwdThreads) {
+            for (int c = threadIdx.x; c < C; c += blockDim.x) {
                 const uint4 gv = ld_stream16(grow + (size_t)c * 8);
                 const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
                 float g[8];
@@ -101,15 +116,30 @@ __global__ void __launch_bounds__(kBwdThreads) combine_backward_kernel(
                         continue;
                     const float wj = s_w[j];
                     const uint32_t yv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                    uint4 o;
-                    uint32_t *ov = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         dot[u] = fmaf(g[2 * i], bf16_lo(yv[i]), dot[u]);
                         dot[u] = fmaf(g[2 * i + 1], bf16_hi(yv[i]), dot[u]);
-                        ov[i] = pack_bf16x2(exact_product_for_bf16(wj, g[2 * i]),
-                                            exact_product_for_bf16(wj, g[2 * i + 1]));
                     }
+                    // Products; a bf16 rounding midpoint among them (low 16
+                    // bits 0x8000, about one in 2^16) takes the exact path.
+                    float pr[8];
+                    uint32_t mid = 0xFFFFu;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        pr[i] = wj * g[i];
+                        mid = min(mid, (__float_as_uint(pr[i]) & 0xFFFFu) ^ 0x8000u);
+                    }
+                    if (mid == 0u) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            pr[i] = exact_product_for_bf16(wj, g[i]);
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(pr[0], pr[1]);
+                    o.y = pack_bf16x2(pr[2], pr[3]);
+                    o.z = pack_bf16x2(pr[4], pr[5]);
+                    o.w = pack_bf16x2(pr[6], pr[7]);
                     st_plain16(grad_y + (size_t)p * H + (size_t)c * 8, o);
                 }
             }
@@ -127,7 +157,7 @@ __global__ void __launch_bounds__(kBwdThreads) combine_backward_kernel(
             if (threadIdx.x < kSlotBatch && j0 + threadIdx.x < k) {
                 const int j = j0 + threadIdx.x;
                 float d = 0.0f;
-                for (int wi = 0; wi < kBwdWarps; ++wi)
+                for (int wi = 0; wi < nwarps; ++wi)
                     d += s_part[threadIdx.x][wi];
                 grad_w[(size_t)t * k + j] = s_pos[j] >= 0 ? d : 0.0f;
             }
@@ -144,17 +174,11 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
 {
     if (T == 0)
         return cudaSuccess;
-    static int per_sm = 0;
-    if (per_sm < 1) {
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_backward_kernel, kBwdThreads, 0);
-        if (per_sm < 1)
-            per_sm = 1;
-    }
-    int grid = device_sm_count() * per_sm;
-    if (grid > T)
-        grid = T;
-    combine_backward_kernel<<<grid, kBwdThreads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y, grad_w, rows,
-                                                          err_flag);
+    const int threads = chunk_threads(H / 8, k);  // <= kBwdThreads (k <= 64)
+    static int cached_threads = 0, cached_per_sm = 0;
+    const int grid = row_grid((const void *)combine_backward_kernel, threads, T, cached_threads, cached_per_sm);
+    combine_backward_kernel<<<grid, threads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y, grad_w, rows,
+                                                      err_flag);
     return cudaGetLastError();
 }
 

@@ -33,6 +33,38 @@ constexpr int kCombThreads = 256;
 constexpr int kMaxK = 64;
 constexpr int kSlotBatch = 8;
 
+}  // namespace
+
+// Threads per CTA for a row of c column chunks and k slots: the fewest
+// passes of at most kCombThreads threads, spread evenly over whole warps
+// (H = 7168: 896 BF16 chunks = 4 passes of 224, not 3.5 passes of 256), and
+// never fewer threads than slots (thread j < k loads slot j's row and
+// weight).
+int chunk_threads(int c, int k)
+{
+    const int passes = (c + kCombThreads - 1) / kCombThreads;
+    const int per_pass = (c + passes - 1) / passes;
+    const int t = ((per_pass + 31) / 32) * 32;
+    const int tk = ((k + 31) / 32) * 32;
+    return t > tk ? t : tk;
+}
+
+// A persistent grid of every resident CTA of the kernel at this block size
+// (at most one per row), the occupancy cached for the last size asked.
+int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cached_per_sm)
+{
+    if (cached_threads != threads) {
+        int per_sm = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+        cached_per_sm = per_sm < 1 ? 1 : per_sm;
+        cached_threads = threads;
+    }
+    const long long g = (long long)device_sm_count() * cached_per_sm;
+    return (int)(g < T ? g : T);
+}
+
+namespace {
+
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *__restrict__ y,
                                                                const int32_t *__restrict__ pos,
                                                                const float *__restrict__ w, int T, int H, int k,

@@ -12,37 +12,43 @@ namespace {
 constexpr long long kGridSpinLimit = 1LL << 21;
 
 // All CTAs of a cooperative grid arrive once; the wait is bounded.
-// word[0] counts arrivals, word[1] is a generation number: the last CTA to
-// arrive resets the count and advances the generation, which releases the
-// others -- so the barrier leaves its two words ready for the next launch.
-// Returns false, with EP_FLAG_TIMEOUT set, if the limit ran out (the words
-// are then left mid-barrier and must be zeroed again).
-__device__ __forceinline__ bool grid_barrier(unsigned *word, unsigned expected, long long spin_limit, int32_t *err_flag)
+// word[0] counts arrivals and is zero when the launch starts.  Each CTA adds
+// one with acquire-release semantics (its writes, and those its threads made
+// before the block barrier, become visible first) and learns its arrival
+// number n.  The last to arrive (n == expected) puts the count back to zero
+// with another read-modify-write, so the word is ready for the next launch
+// with no clearing in between, and an acquire load of either value sees
+// every CTA's writes.  The others poll the count with acquire loads until it
+// equals `expected` or drops below n (the reset: every CTA has arrived; the
+// count only grows until then, and the next launch cannot start before this
+// one ends).  Returns false, with EP_FLAG_TIMEOUT set, if the limit ran out
+// (the count is then left non-zero and must be cleared again; a count that
+// was not zero at launch runs out the same way, unless it was below
+// `expected`).
+__device__ __forceinline__ bool grid_barrier(unsigned *word, unsigned expected, long long spin_limit,
+                                             int32_t *err_flag)
 {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
-        unsigned *count = word, *gen = word + 1;
-        unsigned g0;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(gen) : "memory");
-        __threadfence();  // this CTA's global writes before its arrival
-        const unsigned arrived = atomicAdd(count, 1u) + 1u;
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(word) : "memory");
+        const unsigned n = old + 1u;
         bool ok = true;
-        if (arrived == expected) {
-            // release the others first; the count only has to be back at
-            // zero before the next launch, which starts after this one ends
-            atomicAdd(gen, 1u);
-            atomicExch(count, 0u);
+        if (n == expected) {
+            unsigned prev;  // a read-modify-write: it continues every arrival's release sequence
+            asm volatile("atom.exch.acq_rel.gpu.global.b32 %0, [%1], 0;" : "=r"(prev) : "l"(word) : "memory");
         } else {
-            unsigned g = g0;
-            long long it = 0;
-            for (;;) {
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(gen) : "memory");
-                if (g != g0 || ++it >= spin_limit)
+            ok = false;
+            for (long long it = 0; it < spin_limit; ++it) {
+                unsigned c;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(word) : "memory");
+                if (c == expected || c < n) {
+                    ok = true;
                     break;
+                }
                 __nanosleep(32);
             }
-            ok = g != g0;
         }
         s_ok = ok;
         if (!ok && err_flag)

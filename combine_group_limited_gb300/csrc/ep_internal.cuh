@@ -165,4 +165,8 @@ cudaError_t launch_route(const float *scores, const float *bias, const GateParam
 
 int device_sm_count();
 
+// Launch shape of the CTA-per-row kernels (defined in combine.cu).
+int chunk_threads(int c, int k);
+int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cached_per_sm);
+
 }  // namespace ep

@@ -565,9 +565,8 @@ int layout_num_tiles(int T, int k)
     return (T + tt - 1) / tt;
 }
 
-// Workspace: 256 bytes whose first 8 are the single-launch path's grid
-// barrier words (arrival count, generation; no other path touches them), then
-// either the per-tile
+// Workspace: 256 bytes whose first 4 are the single-launch path's grid
+// barrier count (no other path touches them), then either the per-tile
 // counts of the three-launch path or the per-CTA rows of the single-launch
 // one.
 size_t layout_workspace_bytes(int T, int k, int E, int epr)
@@ -617,7 +616,7 @@ cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int
     }
     if (!capped && route_supported(T, k, E)) {
         // one cooperative launch; its barrier's arrival count starts at zero
-        cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(unsigned), st);
+        cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned), st);
         if (e != cudaSuccess)
             return e;
         return launch_route(nullptr, nullptr, nullptr, topk_idx, nullptr, nullptr, T, k, E, epr, expert_count,

@@ -10,8 +10,9 @@
 //   1. each CTA owns a contiguous range of whole tokens; with gating on it
 //      gates them (gate_impl.cuh), else it reads their chosen experts;
 //   2. it counts its entries per expert in per-warp shared counters (ballot
-//      peer masks; no atomics), turns them into per-warp offsets, counts its
-//      distinct tokens per rank, and publishes its per-expert count row;
+//      peer masks; no atomics), turns them into per-warp offsets (a warp scan
+//      per expert), counts its distinct tokens per rank, and publishes its
+//      per-expert count row;
 //   3. a grid barrier (bounded wait; past its limit EP_FLAG_TIMEOUT);
 //   4. it sums the count rows of the CTAs before it and of all CTAs (16-byte
 //      loads through L2), scans the totals into expert offsets and gives
@@ -32,6 +33,8 @@ constexpr int kRtChunks = 4;                            // 32-entry chunks per w
 constexpr int kRtMaxRange = kRtWarps * 32 * kRtChunks;  // entries per CTA
 constexpr int kRtMaxExperts = 1024;                     // == kRtThreads: one thread per expert in the scan
 constexpr int kRtMaxCtas = 160;
+constexpr int kRtWhStride = kRtWarps + 1;  // per-expert row of per-warp counts, padded against bank conflicts
+constexpr int kRtMaxPhases = 32;           // CTA rows summed per thread in the column sums: C / phases
 
 struct RouteArgs {
     const float *scores;
@@ -49,6 +52,13 @@ struct RouteArgs {
 };
 
 __host__ __device__ inline int round4(int v) { return (v + 3) & ~3; }
+
+// Threads per 4-expert column in the column sums.
+__host__ __device__ inline int route_phases(int E4)
+{
+    const int p = kRtThreads / (E4 / 4);
+    return p < kRtMaxPhases ? p : kRtMaxPhases;
+}
 
 template <bool kGate, int EPL>
 __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
@@ -77,13 +87,13 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
 
     int32_t *s_rt = rsm;                   // [R] this range's distinct tokens per rank
     int32_t *s_rk = s_rt + R;              // [n] rank of each entry of the range (-1: none)
-    int32_t *s_wh = s_rk + n;              // [kRtWarps][E] per-warp counts, then row bases
-    int32_t *s_pre = s_wh + kRtWarps * E;  // [E4] entries of earlier CTAs
-    int32_t *s_tot = s_pre + E4;           // [E4] all entries, then expert offsets
-    int4 *s_part = reinterpret_cast<int4 *>(rsm + round4(R + n + kRtWarps * E + 2 * E4));
+    int32_t *s_wh = s_rk + n;                 // [E][kRtWhStride] per-warp counts, then row bases
+    int32_t *s_pre = s_wh + kRtWhStride * E;  // [E4] entries of earlier CTAs
+    int32_t *s_tot = s_pre + E4;              // [E4] all entries, then expert offsets
+    int4 *s_part = reinterpret_cast<int4 *>(rsm + round4(R + n + kRtWhStride * E + 2 * E4));
     for (int i = threadIdx.x; i < R; i += blockDim.x)
         s_rt[i] = 0;
-    for (int i = threadIdx.x; i < kRtWarps * E; i += blockDim.x)
+    for (int i = threadIdx.x; i < kRtWhStride * E; i += blockDim.x)
         s_wh[i] = 0;
 
     // each warp owns a contiguous slice of at most kRtChunks x 32 entries
@@ -97,9 +107,9 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
     }
     __syncthreads();
 
-    // 2. per-warp counts (a warp's own row: no atomics) and entry ranks
+    // 2. per-warp counts (a warp's own column: no atomics) and entry ranks
     const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
-    int32_t *my = s_wh + warp * E;
+    int32_t *my = s_wh + warp;  // my[key * kRtWhStride]
     int bad = 0;
 #pragma unroll
     for (int c = 0; c < kRtChunks; ++c) {
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         const int key = ok ? e : E;
         const unsigned grp = peer_mask((unsigned)key, eb);
         if (ok && lane == __ffs(grp) - 1)
-            my[key] += __popc(grp);
+            my[key * kRtWhStride] += __popc(grp);
         if (e != -2)
             s_rk[i] = ok ? e / epr : -1;
         __syncwarp();
@@ -136,18 +146,17 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         }
         warp_count(s_rt, first ? (unsigned)r : 0u, first, rb);
     }
-    // per-warp counts -> exclusive per-warp offsets; publish the CTA's row
-    for (int e = threadIdx.x; e < E4; e += blockDim.x) {
-        int base = 0;
-        if (e < E) {
-            for (int w = 0; w < kRtWarps; ++w) {
-                const int c = s_wh[w * E + e];
-                s_wh[w * E + e] = base;
-                base += c;
-            }
-        }
-        a.rows[(size_t)cta * E4 + e] = base;
+    // per-warp counts -> exclusive per-warp offsets (a warp scan per
+    // expert, lane w = warp w's count); publish the CTA's row
+    for (int e = warp; e < E; e += kRtWarps) {
+        const int c = s_wh[e * kRtWhStride + lane];
+        const int incl = warp_incl_scan(c, lane);
+        s_wh[e * kRtWhStride + lane] = incl - c;
+        if (lane == 31)
+            a.rows[(size_t)cta * E4 + e] = incl;
     }
+    for (int e = E + threadIdx.x; e < E4; e += blockDim.x)
+        a.rows[(size_t)cta * E4 + e] = 0;
 
     // 3. every CTA's row is published
     if (!grid_barrier(a.barrier, (unsigned)C, a.spin_limit, a.err_flag))
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
 
     // 4. sums over the rows of the CTAs before this one, and of all
     const int G4 = E4 / 4;
-    const int P = kRtThreads / G4;  // row phases
+    const int P = route_phases(E4);  // threads per column, each summing every P-th row
     int4 *s_pp = s_part, *s_pt = s_part + P * G4;
     if ((int)threadIdx.x < P * G4) {
         const int g = threadIdx.x % G4, ph = threadIdx.x / G4;
@@ -187,6 +196,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int g = e >> 2, q = e & 3;
         int pre = 0, tot = 0;
+#pragma unroll 8
         for (int ph = 0; ph < P; ++ph) {
             pre += reinterpret_cast<const int32_t *>(s_pp + ph * G4 + g)[q];
             tot += reinterpret_cast<const int32_t *>(s_pt + ph * G4 + g)[q];
@@ -241,11 +251,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         if (s_rt[r])
             atomicAdd(a.rank_tokens + r, s_rt[r]);
     // row bases of each warp: offset + earlier CTAs + earlier warps
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int base = s_tot[e] + s_pre[e];
-        for (int w = 0; w < kRtWarps; ++w)
-            s_wh[w * E + e] += base;
-    }
+    for (int e = warp; e < E; e += kRtWarps)
+        s_wh[e * kRtWhStride + lane] += s_tot[e] + s_pre[e];
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         const int key = ok ? e : E;
         const unsigned grp = peer_mask((unsigned)key, eb);
         if (e != -2) {
-            int p = ok ? my[key] + __popc(grp & lt_mask) : -1;
+            int p = ok ? my[key * kRtWhStride] + __popc(grp & lt_mask) : -1;
             if (p >= N)  // unreachable with consistent counts; never write outside src
                 p = -1;
             if (p >= 0)
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         }
         __syncwarp();
         if (ok && lane == __ffs(grp) - 1)
-            my[key] += __popc(grp);
+            my[key * kRtWhStride] += __popc(grp);
         __syncwarp();
     }
 }
@@ -276,8 +283,8 @@ size_t route_smem_bytes(int range, int E, int epr, int warp_floats)
 {
     const int E4 = round4(E);
     const int G4 = E4 / 4;
-    const int P = kRtThreads / G4;
-    const size_t lay = (size_t)round4(E / epr + range + kRtWarps * E + 2 * E4) * sizeof(int32_t) +
+    const int P = route_phases(E4);
+    const size_t lay = (size_t)round4(E / epr + range + kRtWhStride * E + 2 * E4) * sizeof(int32_t) +
                        (size_t)2 * P * G4 * sizeof(int4);
     const size_t gate = (size_t)kRtWarps * warp_floats * sizeof(float);
     return gate > lay ? gate : lay;

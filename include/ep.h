@@ -171,8 +171,7 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
  * workspace     at least ep_layout_workspace_bytes(T, cfg->top_k,
  *               cfg->num_experts, experts_per_rank) bytes, 16-byte aligned,
  *               whose first 4 bytes (the grid barrier's arrival count) are
- *               zero before the call; the next 4 (its generation number)
- *               may hold anything.  Every call that completes leaves the
+ *               zero before the call.  Every call that completes leaves the
  *               count zero (so do ep_get_layout and ep_get_layout_capacity
  *               on the same workspace): clear it once when the workspace is
  *               allocated.  If the barrier's bounded wait runs out,
@@ -341,8 +340,8 @@ ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_row
  * outputs as ep_get_layout; x, H, dtype, recv, recv_rows, recv_scales as
  * ep_dispatch).  1 <= T and T*k <= 4096 (larger batches use the separate
  * calls: EP_ERR_UNSUPPORTED).  workspace: >= 8 bytes of device memory,
- * 4-byte aligned, holding the grid barrier's arrival count and generation:
- * zero it once before the first call; each call leaves it ready for the
+ * 4-byte aligned, whose first 4 bytes hold the grid barrier's arrival count:
+ * zero it once before the first call; each call leaves it zero for the
  * next (calls sharing it must not overlap on the GPU).  The grid barrier
  * between gating and layout waits at most about a second; if that ran out,
  * EP_FLAG_TIMEOUT is set in *err_flag, the outputs are incomplete and the

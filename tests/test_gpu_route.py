@@ -57,8 +57,8 @@ def test_gate_layout_matches_oracle_and_separate_calls(ep, name, T):
 
 
 def test_gate_layout_repeated_on_one_workspace(ep):
-    """The barrier's arrival count is left clear (the generation word moves
-    on), so a workspace is reused as is."""
+    """The barrier's arrival count is left clear, so a workspace is reused
+    as is."""
     cfg = synth.config("dsv3")
     s, b = dev(synth.make_scores(cfg)), dev(synth.make_bias(cfg))
     gc = ep_cfg(ep, cfg)
