@@ -160,19 +160,31 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
     __shared__ float s_w[kMaxK];
     const int C16 = H / 16;
     const int nb = kMx ? H / 32 : H / 128;
+    const bool loader = threadIdx.x < k;  // k <= 64 < blockDim.x
+    int np = -1;
+    float nw = 0.0f;
+    if (loader && blockIdx.x < T) {
+        np = __ldg(pos + (size_t)blockIdx.x * k + threadIdx.x);
+        nw = __ldg(w + (size_t)blockIdx.x * k + threadIdx.x);
+    }
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
-        if (threadIdx.x < k) {
-            int p = __ldg(pos + (size_t)t * k + threadIdx.x);
+        if (loader) {
+            int p = np;
             if (p >= rows) {
                 if (err_flag)
                     atomicOr(err_flag, 2);
                 p = -1;
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+            s_w[threadIdx.x] = nw;
         }
         __syncthreads();
+        const int tn = t + gridDim.x;  // the next token's rows and weights load while this one is summed
+        if (loader && tn < T) {
+            np = __ldg(pos + (size_t)tn * k + threadIdx.x);
+            nw = __ldg(w + (size_t)tn * k + threadIdx.x);
+        }
         for (int c = threadIdx.x; c < C16; c += kCombThreads) {
             float acc[16];
 #pragma unroll
