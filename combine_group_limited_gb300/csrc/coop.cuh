@@ -38,6 +38,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned *word, unsigned expected, 
         if (n == expected) {
             unsigned prev;  // a read-modify-write: it continues every arrival's release sequence
             asm volatile("atom.exch.acq_rel.gpu.global.b32 %0, [%1], 0;" : "=r"(prev) : "l"(word) : "memory");
+            (void)prev;
         } else {
             ok = false;
             for (long long it = 0; it < spin_limit; ++it) {
