@@ -8,7 +8,10 @@
 // FP8 et MXFP8": an FP8 payload halves the bytes against BF16.
 //
 // HBM-bound: every source row is read once and written k times (BF16: 2H
-// bytes in, 2Hk out; FP8: 2H in, k(H + H/32) out).  Work is split into warp
+// bytes in, 2Hk out; FP8: 2H in, k(H + H/32) out).  The standalone calls use
+// the bulk-copy kernel below (rows staged in shared memory, copies issued as
+// cp.async.bulk transfers); rows too long to stage, and the fused decode
+// path, use the warp-item bodies.  Warp-item path: work is split into warp
 // items -- one token's row segment of 32 lanes x 16 bytes (x U) -- handed out
 // grid-stride to a persistent grid of (resident CTAs per SM) x (SMs).  There
 // is no block barrier: lane j of the warp holds the token's j-th receive row
@@ -74,6 +77,165 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_mxfp8_kernel(const uint
     }
 }
 
+// Bulk-copy dispatch: a CTA stages one token's receive row in shared memory
+// (the BF16 row as is, or its FP8 / MXFP8 codes and scales, computed there
+// once), then one thread issues the k copies as cp.async.bulk
+// shared->global transfers -- whole rows handed to the copy engine instead
+// of 16-byte stores from every lane.  Two staging buffers alternate, so the
+// next token is loaded and quantised while the previous token's copies are
+// in flight (a bulk group is waited for, reads only, before its buffer is
+// reused).  Scale rows that are not a multiple of 16 bytes, or whose buffer
+// is not 16-byte aligned, are written with plain stores instead.
+constexpr int kBulkThreads = 256;
+constexpr int kBulkMaxK = 64;
+
+__device__ __forceinline__ void bulk_s2g(void *dst, unsigned src_smem, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+template <int kMode>  // 0: BF16, 1: FP8 e4m3 1x128 (fp32 scales), 2: MXFP8 1x32 (E8M0 scales)
+__global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                                      int k, const int32_t *__restrict__ pos,
+                                                                      uint8_t *__restrict__ recv,
+                                                                      uint8_t *__restrict__ recv_sc, int bulk_sc,
+                                                                      long long rows, int32_t *__restrict__ err_flag)
+{
+    extern __shared__ __align__(128) unsigned char bsm[];
+    __shared__ int32_t s_pos[2][kBulkMaxK];
+    const int row_bytes = kMode == 0 ? 2 * H : H;
+    const int nsc = kMode == 1 ? H / 128 : H / 32;        // scales per row
+    const int sc_bytes = kMode == 0 ? 0 : H / 32;         // fp32 per 128 columns or one byte per 32
+    const int stage = row_bytes + ((sc_bytes + 15) & ~15);
+    int buf = 0;
+    for (long long t = blockIdx.x; t < T; t += gridDim.x, buf ^= 1) {
+        unsigned char *row = bsm + (size_t)buf * stage;
+        unsigned char *sc = row + row_bytes;
+        // this buffer was last read by the copies of two tokens ago
+        if (threadIdx.x == 0)
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        if ((int)threadIdx.x < k) {
+            int p = __ldg(pos + t * k + threadIdx.x);
+            if (p >= rows) {
+                if (err_flag)
+                    atomicOr(err_flag, 2);
+                p = -1;
+            }
+            s_pos[buf][threadIdx.x] = p;
+        }
+        const uint16_t *xrow = x + (size_t)t * H;
+        if (kMode == 0) {
+            for (int c = threadIdx.x; c < H / 8; c += kBulkThreads)
+                reinterpret_cast<uint4 *>(row)[c] = ld_stream16(xrow + (size_t)c * 8);
+        } else {
+            const int C16 = H / 16;
+            for (int c0 = 0; c0 < C16; c0 += kBulkThreads) {  // whole warps in every pass
+                const int c = c0 + threadIdx.x;
+                const bool act = c < C16;
+                if (kMode == 1) {
+                    float sv;
+                    const uint4 q = fp8_quant16(xrow, c, act, sv);
+                    if (act) {
+                        reinterpret_cast<uint4 *>(row)[c] = q;
+                        if ((c & 7) == 0)
+                            reinterpret_cast<float *>(sc)[c >> 3] = sv;
+                    }
+                } else {
+                    uint8_t ev;
+                    const uint4 q = mx_quant16(xrow, c, act, ev);
+                    if (act) {
+                        reinterpret_cast<uint4 *>(row)[c] = q;
+                        if ((c & 1) == 0)
+                            sc[c >> 1] = ev;
+                    }
+                }
+            }
+        }
+        // the staged row is read by the copy engine (the async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned srow = (unsigned)__cvta_generic_to_shared(row);
+            const unsigned ssc = (unsigned)__cvta_generic_to_shared(sc);
+            for (int j = 0; j < k; ++j) {
+                const int p = s_pos[buf][j];
+                if (p < 0)
+                    continue;
+                bulk_s2g(recv + (size_t)p * row_bytes, srow, (unsigned)row_bytes);
+                if (kMode != 0 && bulk_sc)
+                    bulk_s2g(recv_sc + (size_t)p * sc_bytes, ssc, (unsigned)sc_bytes);
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        if (kMode != 0 && !bulk_sc) {
+            for (int i = threadIdx.x; i < k * nsc; i += kBulkThreads) {
+                const int j = i / nsc, b = i - j * nsc;
+                const int p = s_pos[buf][j];
+                if (p < 0)
+                    continue;
+                if (kMode == 1)
+                    reinterpret_cast<float *>(recv_sc)[(size_t)p * nsc + b] = reinterpret_cast<const float *>(sc)[b];
+                else
+                    recv_sc[(size_t)p * nsc + b] = sc[b];
+            }
+        }
+    }
+    // the copies must have completed (written, not only read) before exit
+    if (threadIdx.x == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Staging bytes of the bulk-copy kernel (two rows plus their scales).
+size_t bulk_smem(int H, int mode)
+{
+    const size_t row_bytes = mode == 0 ? 2 * (size_t)H : (size_t)H;
+    const size_t sc_bytes = mode == 0 ? 0 : (size_t)H / 32;
+    return 2 * (row_bytes + ((sc_bytes + 15) & ~(size_t)15));
+}
+
+// The bulk-copy kernel pays a staging round trip per token, repaid by the
+// k copies it hands to the copy engine: measured on GB300 it wins at k >= 4
+// on full batches (DeepSeek-V3 and Qwen3 shapes: FP8 3-9 % faster, BF16 up
+// to 4 %) and loses at k = 2 (Mixtral shape) and on decode-sized batches,
+// which keep the warp-item kernels -- as do rows too long to stage twice in
+// shared memory.
+bool use_bulk(int T, int H, int k, int mode)
+{
+    return k >= 4 && T >= 2048 && bulk_smem(H, mode) <= 200 * 1024;
+}
+
+template <int kMode>
+cudaError_t launch_bulk(const uint16_t *x, int T, int H, int k, const int32_t *pos, void *recv, void *recv_sc,
+                        long long rows, int32_t *err_flag, cudaStream_t st)
+{
+    if (T == 0)
+        return cudaSuccess;
+    const int sc_bytes = kMode == 0 ? 0 : H / 32;
+    const size_t smem = bulk_smem(H, kMode);
+    const int bulk_sc = kMode != 0 && sc_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(recv_sc) & 15) == 0;
+    const void *fn = (const void *)dispatch_bulk_kernel<kMode>;
+    static size_t attr_smem = 48 * 1024;  // per mode; raised to the largest staging seen
+    if (smem > attr_smem) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_smem = smem;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBulkThreads, smem);
+    if (e != cudaSuccess)
+        return e;
+    const int cap = kMode == 0 ? 2 : 4;  // CTAs per SM: in flight rows vs. staging latency (measured)
+    per_sm = per_sm < 1 ? 1 : (per_sm > cap ? cap : per_sm);
+    const long long g = (long long)device_sm_count() * per_sm;
+    const int grid = (int)(g < T ? g : T);
+    dispatch_bulk_kernel<kMode><<<grid, kBulkThreads, smem, st>>>(
+        x, T, H, k, pos, static_cast<uint8_t *>(recv), static_cast<uint8_t *>(recv_sc), bulk_sc, rows, err_flag);
+    return cudaGetLastError();
+}
+
 // A persistent grid of (resident CTAs per SM) x (SMs), capped by the work.
 int persistent_grid(const void *kernel, int &per_sm_cache, long long warp_items)
 {
@@ -98,6 +260,8 @@ cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const 
 {
     if (T == 0)
         return cudaSuccess;
+    if (use_bulk(T, H, k, 2))
+        return launch_bulk<2>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag, st);
     const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_mxfp8_kernel, g_mx_per_sm, items);
     dispatch_mxfp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
@@ -109,6 +273,8 @@ cudaError_t launch_dispatch_bf16(const uint16_t *x, int T, int H, int k, const i
 {
     if (T == 0)
         return cudaSuccess;
+    if (use_bulk(T, H, k, 0))
+        return launch_bulk<0>(x, T, H, k, pos, recv, nullptr, rows, err_flag, st);
     const long long items = (long long)T * bf16_segs(H);
     const int grid = persistent_grid((const void *)dispatch_bf16_kernel, g_bf16_per_sm, items);
     dispatch_bf16_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv, rows, err_flag);
@@ -120,6 +286,8 @@ cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const in
 {
     if (T == 0)
         return cudaSuccess;
+    if (use_bulk(T, H, k, 1))
+        return launch_bulk<1>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag, st);
     const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, items);
     dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag);

@@ -114,19 +114,12 @@ __device__ __forceinline__ void dispatch_bf16_item(const uint16_t *__restrict__ 
     }
 }
 
-// FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.
-__device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
-                                                  int p0, int p1, uint8_t *__restrict__ recv_q,
-                                                  float *__restrict__ recv_s)
+// FP8 e4m3 with one fp32 scale per 128 columns: the codes of the 16 columns
+// [16c, 16c + 16) of row xrow and their block's scale s = amax / 448.  Eight
+// consecutive lanes cover a block: every lane of the warp calls this (lanes
+// with act == false contribute zeros).
+__device__ __forceinline__ uint4 fp8_quant16(const uint16_t *__restrict__ xrow, int c, bool act, float &s_out)
 {
-    const int lane = threadIdx.x & 31;
-    const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
-    const int nb = H / 128;  // scales per row
-    ItemPos it{t, seg};
-    const uint16_t *xrow = x + (size_t)it.t * H;
-    const int c = it.seg * 32 + lane;
-    // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
-    const bool act = c < C16;
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
     if (act) {
         a = ld_stream16(xrow + (size_t)c * 16);
@@ -164,7 +157,25 @@ __device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x
             q[i] = lo | (hi << 16);
         }
     }
-    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+    s_out = s;
+    return make_uint4(q[0], q[1], q[2], q[3]);
+}
+
+// FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.
+__device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
+                                                  int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                  float *__restrict__ recv_s)
+{
+    const int lane = threadIdx.x & 31;
+    const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
+    const int nb = H / 128;  // scales per row
+    ItemPos it{t, seg};
+    const uint16_t *xrow = x + (size_t)it.t * H;
+    const int c = it.seg * 32 + lane;
+    // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
+    const bool act = c < C16;
+    float s;
+    const uint4 qv = fp8_quant16(xrow, c, act, s);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)
@@ -175,18 +186,11 @@ __device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x
     }
 }
 
-// MXFP8: two lanes per 32-column block, E8M0 scale byte.
-__device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,
-                                                    int seg, int p0, int p1, uint8_t *__restrict__ recv_q,
-                                                    uint8_t *__restrict__ recv_e)
+// MXFP8 (E4M3 elements, E8M0 scale per 32 columns): the codes of the 16
+// columns [16c, 16c + 16) and their block's scale byte.  Two consecutive
+// lanes cover a block: every lane of the warp calls this.
+__device__ __forceinline__ uint4 mx_quant16(const uint16_t *__restrict__ xrow, int c, bool act, uint8_t &e_out)
 {
-    const int lane = threadIdx.x & 31;
-    const int C16 = H / 16;  // 16-column groups per row; 2 per 32-column block
-    const int nb = H / 32;   // scale bytes per row
-    ItemPos it{t, seg};
-    const uint16_t *xrow = x + (size_t)it.t * H;
-    const int c = it.seg * 32 + lane;
-    const bool act = c < C16;  // C16 is even: lane pairs are wholly in or out
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
     if (act) {
         a = ld_stream16(xrow + (size_t)c * 16);
@@ -217,8 +221,23 @@ __device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__
         const uint32_t hi = pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
         q[i] = lo | (hi << 16);
     }
-    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-    const uint8_t eb = (uint8_t)(e + 127);
+    e_out = (uint8_t)(e + 127);
+    return make_uint4(q[0], q[1], q[2], q[3]);
+}
+
+// MXFP8: two lanes per 32-column block, E8M0 scale byte.
+__device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,
+                                                    int seg, int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                    uint8_t *__restrict__ recv_e)
+{
+    const int lane = threadIdx.x & 31;
+    const int nb = H / 32;  // scale bytes per row
+    ItemPos it{t, seg};
+    const uint16_t *xrow = x + (size_t)it.t * H;
+    const int c = it.seg * 32 + lane;
+    const bool act = c < H / 16;  // H / 16 is even: lane pairs are wholly in or out
+    uint8_t eb;
+    const uint4 qv = mx_quant16(xrow, c, act, eb);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)

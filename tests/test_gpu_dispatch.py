@@ -144,3 +144,58 @@ def test_dispatch_bad_rows_are_flagged_and_skipped(ep, dtype):
         np.testing.assert_array_equal(q.cpu().numpy(), rq)
     assert _guards_ok(buf)
     assert int(flag.item()) == 2
+
+
+@pytest.mark.parametrize("T,H,k,dtype,scale_offset", [
+    (2048, 384, 4, "fp8", 0),      # 12-byte scale rows: plain scale stores
+    (2048, 7168, 8, "fp8", 4),     # scale buffer 4 bytes off a 16-byte boundary: plain scale stores
+    (2500, 96, 5, "mxfp8", 0),     # 3-byte E8M0 rows
+    (2049, 1024, 6, "mxfp8", 0),   # 32-byte E8M0 rows: bulk copies
+    (3000, 256, 7, "bf16", 0),
+])
+def test_bulk_copy_dispatch_shapes(ep, T, H, k, dtype, scale_offset):
+    """Batches the bulk-copy kernel takes (k >= 4, T >= 2048): each token's
+    row staged in shared memory and written by cp.async.bulk copies, scale
+    rows by bulk copies or, when short or unaligned, by plain stores; empty
+    slots leave their rows untouched and guard bytes survive."""
+    rng = np.random.default_rng(T * k + H)
+    x = synth.f32_to_bf16_bits((rng.normal(0, 1, (T, H)) * np.exp2(rng.integers(-8, 8, (T, 1)))).astype(np.float32))
+    rows = T * k
+    pos = rng.permutation(rows).reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.1] = -1
+    xd, pd = dev_bf16(x), dev(pos)
+    if dtype == "bf16":
+        buf, body = _guarded(rows * H * 2)
+        recv = body.view(torch.bfloat16).view(rows, H)
+        ep.ep_dispatch(xd, pd, "bf16", recv=recv)
+        torch.cuda.synchronize()
+        ref = np.full((rows, H), 0xA5A5, np.uint16)
+        oracle.dispatch_bf16(x, pos, recv=ref)
+        np.testing.assert_array_equal(host_bits(recv), ref)
+        assert _guards_ok(buf)
+        return
+    nsb = H // 128 * 4 if dtype == "fp8" else H // 32          # scale bytes per row
+    buf, body = _guarded(rows * H)
+    sbuf, sraw = _guarded(rows * nsb + 16)
+    sbody = sraw[scale_offset:scale_offset + rows * nsb]
+    q = body.view(rows, H)
+    if dtype == "fp8":
+        s = sbody.view(torch.float32).view(rows, H // 128)
+        ep.ep_dispatch(xd, pd, "fp8", recv=q, recv_scales=s)
+        torch.cuda.synchronize()
+        rq = np.full((rows, H), 0xA5, np.uint8)
+        rs = np.full((rows, H // 128), 0xA5A5A5A5, np.uint32).view(np.float32)
+        oracle.dispatch_fp8(x, pos, recv_q=rq, recv_s=rs)
+        np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    else:
+        s = sbody.view(rows, H // 32)
+        ep.ep_dispatch(xd, pd, "mxfp8", recv=q, recv_scales=s)
+        torch.cuda.synchronize()
+        rq = np.full((rows, H), 0xA5, np.uint8)
+        rs = np.full((rows, H // 32), 0xA5, np.uint8)
+        oracle.dispatch_mxfp8(x, pos, recv_q=rq, recv_e=rs)
+        np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    assert _guards_ok(buf)
+    h = sbuf.cpu().numpy()
+    assert np.all(h[:GUARD + scale_offset] == 0xA5) and np.all(h[GUARD + scale_offset + rows * nsb:] == 0xA5)

@@ -52,12 +52,14 @@ def _blocks(B, H, seed):
     return x.reshape(rows, H)
 
 
-@pytest.mark.parametrize("fmt,B", [("fp8", 128), ("mxfp8", 32)])
-def test_every_bf16_value_at_every_relative_scale(ep, fmt, B):
+@pytest.mark.parametrize("fmt,B,k,rep", [("fp8", 128, 2, 1), ("mxfp8", 32, 2, 1), ("fp8", 128, 4, 13),
+                                          ("mxfp8", 32, 4, 13)])
+def test_every_bf16_value_at_every_relative_scale(ep, fmt, B, k, rep):
+    """rep > 1 repeats the rows up to a batch the bulk-copy kernel takes
+    (T >= 2048, k >= 4); rep = 1 runs the warp-item kernel."""
     H = 4096
-    x = _blocks(B, H, seed=77 + B)
+    x = np.tile(_blocks(B, H, seed=77 + B), (rep, 1))
     T = x.shape[0]
-    k = 2
     pos = np.random.default_rng(5).permutation(T * k).reshape(T, k).astype(np.int32)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, s = ep.ep_dispatch(dev_bf16(x), dev(pos), fmt, err_flag=flag)
