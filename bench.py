@@ -344,7 +344,7 @@ def run_ours(args):
         peak, peak_kind = measured_hbm_peak()
         ab = algorithmic_bytes(cfg)
         bytes_of = {"route": ab["gate"] + ab["layout"], "dispatch": ab["dispatch_fp8"], "combine": ab["combine"]}
-        kname = {"route": "route_kernel", "dispatch": "dispatch_fp8_kernel", "combine": "combine_kernel"}
+        kname = {"route": "route_kernel", "dispatch": "dispatch_bulk_kernel", "combine": "combine_kernel"}
         op_summary = {}
         for op in ops:
             us = 1e3 * statistics.mean(per_op[op])
