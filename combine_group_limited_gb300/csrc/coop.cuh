@@ -36,9 +36,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned *word, unsigned expected, 
         const unsigned n = old + 1u;
         bool ok = true;
         if (n == expected) {
-            unsigned prev;  // a read-modify-write: it continues every arrival's release sequence
-            asm volatile("atom.exch.acq_rel.gpu.global.b32 %0, [%1], 0;" : "=r"(prev) : "l"(word) : "memory");
-            (void)prev;
+            atomicExch(word, 0u);  // a read-modify-write: it continues every arrival's release sequence
         } else {
             ok = false;
             for (long long it = 0; it < spin_limit; ++it) {

@@ -153,7 +153,8 @@ cudaError_t launch_barrier_selftest(unsigned extra, long long spin_limit, int32_
                                     cudaStream_t st);
 
 // Gating (gp != NULL, scores -> topk_idx, topk_w) and/or layout (of
-// topk_idx_in when gp == NULL) in one cooperative launch.  workspace: at
+// topk_idx_in when gp == NULL; capacity mode when cap >= 0, src then cleared
+// to -1 beforehand) in one cooperative launch.  workspace: at
 // least route_workspace_bytes(E), 16-byte aligned; its first word (the grid
 // barrier's arrival count) zero, and left zero by every call that completes.
 size_t route_workspace_bytes(int E);
@@ -161,7 +162,8 @@ bool route_supported(int T, int k, int E);
 cudaError_t launch_route(const float *scores, const float *bias, const GateParams *gp, const int32_t *topk_idx_in,
                          int32_t *topk_idx, float *topk_w, int T, int k, int E, int epr, int32_t *expert_count,
                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
-                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st);
+                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st,
+                         int cap = -1, int32_t *expert_dropped = nullptr);
 
 int device_sm_count();
 

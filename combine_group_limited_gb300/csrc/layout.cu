@@ -8,10 +8,10 @@
 // the host.
 //
 // Batches of up to 4096 entries take one launch (layout_small_kernel).  Larger
-// ones take one cooperative launch (route.cu) while a grid of one CTA per SM
-// covers them with at most 4096 entries per CTA; beyond that (and in
-// capacity mode) they take three launches over tiles of whole tokens (about
-// 512 entries each):
+// ones, and capacity mode, take one cooperative launch (route.cu) while a
+// grid of one CTA per SM covers them with at most 4096 entries per CTA;
+// beyond that they take three launches over tiles of whole tokens (about 512
+// entries each):
 //  1. count:  per tile, per-expert entry counts and per-rank distinct-token
 //             counts (shared-memory integer atomics; the totals do not depend
 //             on their order).  Workspace columns [E][tiles], [R][tiles].
@@ -614,13 +614,14 @@ cudaError_t launch_layout_impl(const int32_t *topk_idx, int T, int k, int E, int
                                                             rank_count, rank_off, rank_tokens, pos, src, err_flag);
         return cudaGetLastError();
     }
-    if (!capped && route_supported(T, k, E)) {
+    if (route_supported(T, k, E) && (capped || T * k > kSmallEntries)) {
         // one cooperative launch; its barrier's arrival count starts at zero
         cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned), st);
         if (e != cudaSuccess)
             return e;
         return launch_route(nullptr, nullptr, nullptr, topk_idx, nullptr, nullptr, T, k, E, epr, expert_count,
-                            expert_off, rank_count, rank_off, rank_tokens, pos, src, err_flag, workspace, st);
+                            expert_off, rank_count, rank_off, rank_tokens, pos, src, err_flag, workspace, st,
+                            capped ? cap : -1, expert_dropped);
     }
     int32_t *ws_cnt = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + 256);
     int32_t *ws_rt = ws_cnt + (size_t)nt * E;

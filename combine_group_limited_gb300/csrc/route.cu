@@ -46,7 +46,9 @@ struct RouteArgs {
     int T, k, E, E4, epr;
     int32_t *expert_count, *expert_off, *rank_count, *rank_off, *rank_tokens, *pos, *src;
     int32_t *err_flag;
-    unsigned *barrier;  // two words, zero at launch
+    int cap;                  // >= 0: capacity mode (expert e owns rows [e*cap, (e+1)*cap)); -1: dropless
+    int32_t *expert_dropped;  // [E], capacity mode
+    unsigned *barrier;  // arrival count, zero at launch
     int32_t *rows;      // [gridDim.x][E4] per-CTA expert counts
     long long spin_limit;
 };
@@ -58,6 +60,87 @@ __host__ __device__ inline int route_phases(int E4)
 {
     const int p = kRtThreads / (E4 / 4);
     return p < kRtMaxPhases ? p : kRtMaxPhases;
+}
+
+// Capacity mode after the column sums (s_tot: every entry per expert; s_pre:
+// entries of earlier CTAs): expert e keeps its first cap entries in flat
+// order, in rows [e*cap, (e+1)*cap); later ones are dropped (pos = -1).
+// src was cleared to -1 before the launch.  Distinct tokens per rank count
+// kept entries only.
+__device__ __forceinline__ void route_place_capped(const RouteArgs &a, const int32_t *s_tot, const int32_t *s_pre,
+                                                   int32_t *s_wh, int32_t *s_rk, int32_t *s_rt,
+                                                   const int (&ev)[kRtChunks], int per_warp, int w0, int n_lo,
+                                                   int eb, int rb)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E, epr = a.epr, R = E / epr, cap = a.cap, k = a.k;
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int tot = s_tot[e], kept = tot < cap ? tot : cap;
+            a.expert_count[e] = kept;
+            a.expert_dropped[e] = tot - kept;
+            a.expert_off[e] = e * cap;
+        }
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            int kept = 0;
+            for (int e = r * epr; e < (r + 1) * epr; ++e)
+                kept += s_tot[e] < cap ? s_tot[e] : cap;
+            a.rank_count[r] = kept;
+            a.rank_off[r] = r * epr * cap;
+        }
+        if (threadIdx.x == 0) {
+            a.expert_off[E] = E * cap;
+            a.rank_off[R] = E * cap;
+        }
+    }
+    // each warp's first rank within the expert: earlier CTAs + earlier warps
+    for (int e = warp; e < E; e += kRtWarps)
+        s_wh[e * kRtWhStride + lane] += s_pre[e];
+    __syncthreads();
+    int32_t *my = s_wh + warp;
+    const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+    for (int c = 0; c < kRtChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int i = w0 + 32 * c + lane;
+        const int e = ev[c];
+        const bool ok = (unsigned)e < (unsigned)E;
+        const int key = ok ? e : E;
+        const unsigned grp = peer_mask((unsigned)key, eb);
+        if (e != -2) {
+            const int rank = ok ? my[key * kRtWhStride] + __popc(grp & lt_mask) : cap;
+            const int p = rank < cap ? key * cap + rank : -1;
+            if (p >= 0)
+                a.src[p] = n_lo + i;
+            else
+                s_rk[i] = -1;  // dropped: no distinct-token count
+            a.pos[n_lo + i] = p;
+        }
+        __syncwarp();
+        if (ok && lane == __ffs(grp) - 1)
+            my[key * kRtWhStride] += __popc(grp);
+        __syncwarp();
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kRtChunks; ++c) {
+        if (32 * c >= per_warp)
+            break;
+        const int i = w0 + 32 * c + lane;
+        const int r = ev[c] != -2 ? s_rk[i] : -1;
+        bool first = r >= 0;
+        if (first) {
+            const int j = i % k;
+            for (int jj = 0; jj < j; ++jj)
+                first &= s_rk[i - j + jj] != r;
+        }
+        warp_count(s_rt, first ? (unsigned)r : 0u, first, rb);
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += blockDim.x)
+        if (s_rt[r])
+            atomicAdd(a.rank_tokens + r, s_rt[r]);
 }
 
 template <bool kGate, int EPL>
@@ -131,10 +214,12 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         atomicOr(a.err_flag, 1);
     __syncthreads();
     // distinct tokens per rank: an entry counts if no earlier slot of its
-    // token is on the same rank (ranges hold whole tokens)
+    // token is on the same rank (ranges hold whole tokens).  In capacity
+    // mode only kept entries count, known after the barrier.
+    const bool capped = a.cap >= 0;
 #pragma unroll
     for (int c = 0; c < kRtChunks; ++c) {
-        if (32 * c >= per_warp)
+        if (32 * c >= per_warp || capped)
             break;
         const int i = w0 + 32 * c + lane;
         const int r = ev[c] != -2 ? s_rk[i] : -1;
@@ -205,6 +290,10 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         s_tot[e] = tot;
     }
     __syncthreads();
+    if (capped) {
+        route_place_capped(a, s_tot, s_pre, s_wh, s_rk, s_rt, ev, per_warp, w0, n_lo, eb, rb);
+        return;
+    }
     // exclusive scan of the totals: one thread per expert
     {
         const int e = threadIdx.x;
@@ -335,9 +424,12 @@ bool route_supported(int T, int k, int E)
 cudaError_t launch_route(const float *scores, const float *bias, const GateParams *gp, const int32_t *topk_idx_in,
                          int32_t *topk_idx, float *topk_w, int T, int k, int E, int epr, int32_t *expert_count,
                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
-                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st)
+                         int32_t *pos, int32_t *src, int32_t *err_flag, void *workspace, cudaStream_t st, int cap,
+                         int32_t *expert_dropped)
 {
     RouteArgs a{};
+    a.cap = gp ? -1 : cap;
+    a.expert_dropped = expert_dropped;
     a.scores = scores;
     a.bias = bias;
     if (gp)

@@ -158,6 +158,26 @@ def test_capacity_layout_extremes_with_skips(ep, cap):
         np.testing.assert_array_equal(got, o[key].reshape(-1), err_msg=key)
 
 
+@pytest.mark.parametrize("T,k,E,epr,cap", [(3000, 6, 64, 8, 200), (100000, 8, 256, 8, 2900)])
+def test_capacity_layout_bad_indices_and_large_batches(ep, T, k, E, epr, cap):
+    """Out-of-range indices are flagged and skipped in capacity mode too;
+    100000 tokens run the three-launch kernels (a grid of one CTA per SM would
+    hold more than 4096 entries per CTA), 3000 the single launch."""
+    rng = np.random.default_rng(T + cap)
+    idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
+    idx[rng.random((T, k)) < 0.002] = E + 3
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = ep.ep_get_layout_capacity(dev(idx), E, epr, cap, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == ep.EP_FLAG_BAD_EXPERT
+    clean = idx.copy()
+    clean[clean >= E] = -1
+    o = oracle.layout_capacity(clean, E, epr, cap)
+    for key in CAP_KEYS:
+        got = getattr(g, key).cpu().numpy().reshape(-1)[: o[key].size]
+        np.testing.assert_array_equal(got, o[key].reshape(-1), err_msg=key)
+
+
 def test_capacity_path_end_to_end(ep):
     """Gate -> capacity layout -> dispatch into E*capacity rows -> combine:
     dropped entries (pos -1) contribute nothing; the rest match the oracle."""

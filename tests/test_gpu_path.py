@@ -37,11 +37,16 @@ def test_bench_step_matches_oracle():
     assert_combine_close(host_bits(r.out), oracle.combine(y, pos, w), y, pos, w)
 
 
-def test_token_chunked_calls_equal_whole_batch():
+@pytest.mark.parametrize("T,bounds", [
+    (1000, [0, 1, 130, 131, 517, 999, 1000]),
+    # whole batch through the bulk-copy dispatch, slices through the warp-item kernel
+    (4096, [0, 512, 1024, 1536, 2048, 2049, 3000, 4096]),
+])
+def test_token_chunked_calls_equal_whole_batch(T, bounds):
     """Dispatch and combine over token slices (as a pipelined caller issues
     them while rows stream in) give the whole-batch results bit for bit."""
     import combine_group_limited_gb300 as ep
-    cfg = synth.config("dsv3", T=1000)
+    cfg = synth.config("dsv3", T=T)
     inp = synth.make_inputs(cfg)
     s = torch.from_numpy(inp["scores"]).cuda()
     b = torch.from_numpy(inp["bias"]).cuda()
@@ -56,9 +61,54 @@ def test_token_chunked_calls_equal_whole_batch():
     q2 = torch.zeros_like(q)
     sc2 = torch.zeros_like(sc)
     out2 = torch.zeros_like(out)
-    bounds = [0, 1, 130, 131, 517, 999, 1000]
     for a, e in zip(bounds, bounds[1:]):
         ep.ep_dispatch(x[a:e], lay.pos[a:e], "fp8", recv=q2, recv_scales=sc2)
         ep.ep_combine(y, lay.pos[a:e], w[a:e], out=out2[a:e])
     torch.cuda.synchronize()
     assert torch.equal(q, q2) and torch.equal(sc, sc2) and torch.equal(out, out2)
+
+
+def test_step_replayed_from_a_cuda_graph_equals_direct_calls():
+    """The step's C-ABI calls captured once in a CUDA graph (as the end-to-end
+    leg of the bench does) and replayed give the results of direct calls."""
+    import combine_group_limited_gb300 as ep
+    cfg = synth.config("dsv3", T=2304)
+    inp = synth.make_inputs(cfg)
+    s = torch.from_numpy(inp["scores"]).cuda()
+    b = torch.from_numpy(inp["bias"]).cuda()
+    x = torch.from_numpy(inp["x"].view(np.int16)).cuda().view(torch.bfloat16)
+    gc = ep.gate_cfg(cfg["E"], cfg["k"], cfg["n_groups"], cfg["topk_group"], cfg["topk_in_group"], cfg["score_fn"],
+                     cfg["normalize"])
+    T, k, E, epr, H = cfg["T"], cfg["k"], cfg["E"], cfg["experts_per_rank"], cfg["H"]
+    idx, w, lay = ep.ep_gate_layout(s, b, gc, epr)
+    y = ep.ep_dispatch(x, lay.pos, "bf16")
+    q, sc = ep.ep_dispatch(x, lay.pos, "fp8")
+    out = ep.ep_combine(y, lay.pos, w)
+    torch.cuda.synchronize()
+    gidx, gw = torch.empty_like(idx), torch.empty_like(w)
+    glay = ep.alloc_layout(T, k, E, epr, "cuda")
+    ws = ep.alloc_layout_workspace(T, k, E, epr)
+    gq, gsc, gout = torch.zeros_like(q), torch.zeros_like(sc), torch.zeros_like(out)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        ep.ep_gate_layout(s, b, gc, epr, topk_idx=gidx, topk_w=gw, out=glay, workspace=ws, err_flag=err)
+        ep.ep_dispatch(x, glay.pos, "fp8", recv=gq, recv_scales=gsc, err_flag=err)
+        ep.ep_combine(y, glay.pos, gw, out=gout, err_flag=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                                    # first calls outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            step()
+        for t in (gq, gsc, gout):
+            t.zero_()
+        g.replay()
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(gidx, idx) and torch.equal(gw, w) and torch.equal(glay.pos, lay.pos)
+    assert torch.equal(gq, q) and torch.equal(gsc, sc) and torch.equal(gout, out)
