@@ -104,10 +104,15 @@ def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     _assert_fp8_combine_close(host_bits(out), r, _dequant(qh, sh, 128 if fmt == "fp8" else 32), pos, wh)
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "mxfp8"])
-def test_combine_fp8_random_codes_signed_weights(ep, fmt):
-    rng = np.random.default_rng(9)
-    T, H, k = 77, 1024, 6
+@pytest.mark.parametrize("fmt,T,H,k,scale_offset", [
+    ("fp8", 77, 1024, 6, 0), ("mxfp8", 77, 1024, 6, 0),
+    # larger batches; short scale rows (H = 384 FP8: 12 bytes, H = 96 MXFP8: 3
+    # bytes); a scale buffer 4 bytes off a 16-byte boundary
+    ("fp8", 2048, 1024, 6, 0), ("mxfp8", 2100, 512, 8, 0), ("fp8", 2048, 384, 4, 0), ("mxfp8", 2049, 96, 5, 0),
+    ("fp8", 2048, 1024, 6, 4),
+])
+def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset):
+    rng = np.random.default_rng(9 + T + H)
     rows = T * k
     q = rng.integers(0, 256, size=(rows, H)).astype(np.uint8)
     q[(q & 0x7F) == 0x7F] = 0x3C
@@ -116,7 +121,12 @@ def test_combine_fp8_random_codes_signed_weights(ep, fmt):
     pos = rng.permutation(rows).reshape(T, k).astype(np.int32)
     pos[rng.random((T, k)) < 0.2] = -1
     w = rng.uniform(-1, 1, (T, k)).astype(np.float32)
-    out = ep.ep_combine_fp8(dev(q), dev(s), dev(pos), dev(w))
+    sb = s.view(np.uint8).reshape(-1)
+    sraw = torch.zeros(sb.size + 16, dtype=torch.uint8, device="cuda")
+    sraw[scale_offset:scale_offset + sb.size] = dev(sb)
+    sd = sraw[scale_offset:scale_offset + sb.size]
+    sd = sd.view(torch.float32).view(s.shape) if fmt == "fp8" else sd.view(s.shape)
+    out = ep.ep_combine_fp8(dev(q), sd, dev(pos), dev(w))
     torch.cuda.synchronize()
     r = oracle.combine_fp8(q, s, pos, w)
     _assert_fp8_combine_close(host_bits(out), r, _dequant(q, s, 128 if fmt == "fp8" else 32), pos, w)
