@@ -185,6 +185,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
             float gs;
             if (p.kin <= 2) {
                 uint32_t a0 = srt[0], a1 = EPL > 1 ? srt[EPL > 1 ? 1 : 0] : 0u;
+#pragma unroll 4
                 for (int off = 1; off < group_lanes; off <<= 1) {
                     const uint32_t b0 = __shfl_xor_sync(kFullMask, a0, off);
                     const uint32_t b1 = __shfl_xor_sync(kFullMask, a1, off);
@@ -218,6 +219,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
             const int my_group = lane / group_lanes;
             const bool leader = (lane % group_lanes) == 0 && my_group < p.G;
             uint32_t kept = 0u;
+#pragma unroll 4
             for (int r = 0; r < p.Kg; ++r) {
                 const bool c = leader && !((kept >> my_group) & 1u);
                 const uint32_t o = c ? ordered_key(gs) : 0u;
@@ -251,6 +253,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
     uint32_t hk = lane_kept ? srt[0] : 0u;
     int h = 0;
     uint32_t won = 0u;  // bit j: this lane won round j
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
         const uint32_t mx = __reduce_max_sync(kFullMask, hk);
         const unsigned bal = __ballot_sync(kFullMask, hk == mx && mx != 0u);
@@ -293,6 +296,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
     if (p.score_fn == 0) {
         if (p.normalize) {
             float den = 0.0f;
+#pragma unroll 8
             for (int jj = 0; jj < k; ++jj)
                 den += __shfl_sync(kFullMask, my_s, jj);
             w = my_s / den;
@@ -306,6 +310,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
             m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
         const float ex = (lane < k) ? expf(my_s - m) : 0.0f;
         float den = 0.0f;
+#pragma unroll 8
         for (int jj = 0; jj < k; ++jj)
             den += __shfl_sync(kFullMask, ex, jj);
         w = ex / den;
