@@ -10,7 +10,8 @@
 // pos (token-major) names the k rows to read.  HBM-bound: 2Hk bytes in and
 // 2H out per token.  A CTA takes one token at a time; a thread owns a
 // 16-byte column chunk and first issues the loads of up to 8 slots, then
-// runs their fmas in order, so eight 16-byte loads are in flight per thread.
+// runs their fmas in order, so eight 16-byte loads are in flight per thread;
+// the next token's rows and weights are fetched while one is summed.
 // With w == NULL every weight is 1: the backward of the BF16 dispatch (a
 // copy), whose source-row gradient is the sum of its copies' gradients.
 //
@@ -74,19 +75,31 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *_
     __shared__ int32_t s_pos[kMaxK];
     __shared__ float s_w[kMaxK];
     const int C = H / 8;
+    const bool loader = threadIdx.x < k;  // k <= 64 < blockDim.x
+    int np = -1;
+    float nw = 0.0f;
+    if (loader && blockIdx.x < T) {
+        np = __ldg(pos + (size_t)blockIdx.x * k + threadIdx.x);
+        nw = w ? __ldg(w + (size_t)blockIdx.x * k + threadIdx.x) : 1.0f;
+    }
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
-        if (threadIdx.x < k) {
-            int p = __ldg(pos + (size_t)t * k + threadIdx.x);
+        if (loader) {
+            int p = np;
             if (p >= rows) {
                 if (err_flag)
                     atomicOr(err_flag, 2);
                 p = -1;
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = w ? __ldg(w + (size_t)t * k + threadIdx.x) : 1.0f;
+            s_w[threadIdx.x] = nw;
         }
         __syncthreads();
+        const int tn = t + gridDim.x;  // the next token's rows and weights load while this one is summed
+        if (loader && tn < T) {
+            np = __ldg(pos + (size_t)tn * k + threadIdx.x);
+            nw = w ? __ldg(w + (size_t)tn * k + threadIdx.x) : 1.0f;
+        }
         for (int c = threadIdx.x; c < C; c += kCombThreads) {
             float acc[8];
 #pragma unroll
