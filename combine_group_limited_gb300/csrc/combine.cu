@@ -50,6 +50,21 @@ int chunk_threads(int c, int k)
     return t > tk ? t : tk;
 }
 
+// Column segments per token for the CTA-per-row kernels: a batch too small
+// to give every resident CTA a token (decode-sized) splits each row into S
+// segments of at least half a pass of kCombThreads chunks, so more CTAs
+// share the rows and each runs fewer dependent passes.
+int column_segments(int T, int chunks, int resident)
+{
+    if (T <= 0 || T >= resident)
+        return 1;
+    int S = (resident + T - 1) / T;
+    const int most = chunks / (kCombThreads / 2);
+    if (S > most)
+        S = most;
+    return S < 1 ? 1 : S;
+}
+
 // A persistent grid of every resident CTA of the kernel at this block size
 // (at most one per row), the occupancy cached for the last size asked.
 int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cached_per_sm)
@@ -66,23 +81,30 @@ int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cac
 
 namespace {
 
+template <bool kSplit>  // false: S == 1 (one item per token, no division per item)
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *__restrict__ y,
                                                                const int32_t *__restrict__ pos,
                                                                const float *__restrict__ w, int T, int H, int k,
                                                                uint16_t *__restrict__ out, long long rows,
-                                                               int32_t *__restrict__ err_flag)
+                                                               int32_t *__restrict__ err_flag, int S)
 {
     __shared__ int32_t s_pos[kMaxK];
     __shared__ float s_w[kMaxK];
     const int C = H / 8;
-    const bool loader = threadIdx.x < k;  // k <= 64 < blockDim.x
+    const long long items = (long long)T * S;  // (token, column segment) pairs
+    const bool loader = threadIdx.x < k;        // k <= 64 < blockDim.x
     int np = -1;
     float nw = 0.0f;
-    if (loader && blockIdx.x < T) {
-        np = __ldg(pos + (size_t)blockIdx.x * k + threadIdx.x);
-        nw = w ? __ldg(w + (size_t)blockIdx.x * k + threadIdx.x) : 1.0f;
+    if (loader && blockIdx.x < items) {
+        const long long t0 = kSplit ? blockIdx.x / S : blockIdx.x;
+        np = __ldg(pos + t0 * k + threadIdx.x);
+        nw = w ? __ldg(w + t0 * k + threadIdx.x) : 1.0f;
     }
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const long long t = kSplit ? it / S : it;
+        const int seg = kSplit ? (int)(it - t * S) : 0;
+        const int c_lo = kSplit ? (int)((long long)C * seg / S) : 0;
+        const int c_hi = kSplit ? (int)((long long)C * (seg + 1) / S) : C;
         __syncthreads();
         if (loader) {
             int p = np;
@@ -95,12 +117,13 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const uint16_t *_
             s_w[threadIdx.x] = nw;
         }
         __syncthreads();
-        const int tn = t + gridDim.x;  // the next token's rows and weights load while this one is summed
-        if (loader && tn < T) {
-            np = __ldg(pos + (size_t)tn * k + threadIdx.x);
-            nw = w ? __ldg(w + (size_t)tn * k + threadIdx.x) : 1.0f;
+        const long long itn = it + gridDim.x;  // the next item's rows and weights load while this one is summed
+        if (loader && itn < items) {
+            const long long tn = kSplit ? itn / S : itn;
+            np = __ldg(pos + tn * k + threadIdx.x);
+            nw = w ? __ldg(w + tn * k + threadIdx.x) : 1.0f;
         }
-        for (int c = threadIdx.x; c < C; c += kCombThreads) {
+        for (int c = c_lo + threadIdx.x; c < c_hi; c += kCombThreads) {
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -161,26 +184,32 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b)
 }
 
 // kMx: scales are E8M0 bytes per 32 columns; else fp32 per 128 columns.
-template <bool kMx>
+template <bool kMx, bool kSplit>
 __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t *__restrict__ yq,
                                                                    const void *__restrict__ yscale,
                                                                    const int32_t *__restrict__ pos,
                                                                    const float *__restrict__ w, int T, int H, int k,
                                                                    uint16_t *__restrict__ out, long long rows,
-                                                                   int32_t *__restrict__ err_flag)
+                                                                   int32_t *__restrict__ err_flag, int S)
 {
     __shared__ int32_t s_pos[kMaxK];
     __shared__ float s_w[kMaxK];
     const int C16 = H / 16;
     const int nb = kMx ? H / 32 : H / 128;
-    const bool loader = threadIdx.x < k;  // k <= 64 < blockDim.x
+    const long long items = (long long)T * S;  // (token, column segment) pairs
+    const bool loader = threadIdx.x < k;        // k <= 64 < blockDim.x
     int np = -1;
     float nw = 0.0f;
-    if (loader && blockIdx.x < T) {
-        np = __ldg(pos + (size_t)blockIdx.x * k + threadIdx.x);
-        nw = __ldg(w + (size_t)blockIdx.x * k + threadIdx.x);
+    if (loader && blockIdx.x < items) {
+        const long long t0 = kSplit ? blockIdx.x / S : blockIdx.x;
+        np = __ldg(pos + t0 * k + threadIdx.x);
+        nw = __ldg(w + t0 * k + threadIdx.x);
     }
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const long long t = kSplit ? it / S : it;
+        const int seg = kSplit ? (int)(it - t * S) : 0;
+        const int c_lo = kSplit ? (int)((long long)C16 * seg / S) : 0;
+        const int c_hi = kSplit ? (int)((long long)C16 * (seg + 1) / S) : C16;
         __syncthreads();
         if (loader) {
             int p = np;
@@ -193,12 +222,13 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
             s_w[threadIdx.x] = nw;
         }
         __syncthreads();
-        const int tn = t + gridDim.x;  // the next token's rows and weights load while this one is summed
-        if (loader && tn < T) {
-            np = __ldg(pos + (size_t)tn * k + threadIdx.x);
-            nw = __ldg(w + (size_t)tn * k + threadIdx.x);
+        const long long itn = it + gridDim.x;  // the next item's rows and weights load while this one is summed
+        if (loader && itn < items) {
+            const long long tn = kSplit ? itn / S : itn;
+            np = __ldg(pos + tn * k + threadIdx.x);
+            nw = __ldg(w + tn * k + threadIdx.x);
         }
-        for (int c = threadIdx.x; c < C16; c += kCombThreads) {
+        for (int c = c_lo + threadIdx.x; c < c_hi; c += kCombThreads) {
             float acc[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -264,16 +294,20 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
 {
     if (T == 0)
         return cudaSuccess;
-    static int per_sm = 0;
+    static int per_sm = 0;  // the same registers either way: sized on the unsplit kernel
     if (per_sm < 1) {
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_kernel, kCombThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_kernel<false>, kCombThreads, 0);
         if (per_sm < 1)
             per_sm = 1;
     }
-    int grid = device_sm_count() * per_sm;
-    if (grid > T)
-        grid = T;
-    combine_kernel<<<grid, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag);
+    const int S = column_segments(T, H / 8, device_sm_count() * per_sm);
+    long long grid = (long long)device_sm_count() * per_sm;
+    if (grid > (long long)T * S)
+        grid = (long long)T * S;
+    if (S > 1)
+        combine_kernel<true><<<(int)grid, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag, S);
+    else
+        combine_kernel<false><<<(int)grid, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag, 1);
     return cudaGetLastError();
 }
 
@@ -287,20 +321,31 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
     if (T == 0)
         return cudaSuccess;
     static int per_sm_cache[2] = {0, 0};
-    const void *kern = mx ? (const void *)combine_fp8_kernel<true> : (const void *)combine_fp8_kernel<false>;
+    const void *kern =
+        mx ? (const void *)combine_fp8_kernel<true, false> : (const void *)combine_fp8_kernel<false, false>;
     int &per_sm = per_sm_cache[mx ? 1 : 0];
     if (per_sm < 1) {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombThreads, 0);
         if (per_sm < 1)
             per_sm = 1;
     }
-    int grid = device_sm_count() * per_sm;
-    if (grid > T)
-        grid = T;
-    if (mx)
-        combine_fp8_kernel<true><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows, err_flag);
+    const int S = column_segments(T, H / 16, device_sm_count() * per_sm);
+    long long gl = (long long)device_sm_count() * per_sm;
+    if (gl > (long long)T * S)
+        gl = (long long)T * S;
+    const int grid = (int)gl;
+    if (mx && S > 1)
+        combine_fp8_kernel<true, true><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                      err_flag, S);
+    else if (mx)
+        combine_fp8_kernel<true, false><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                       err_flag, 1);
+    else if (S > 1)
+        combine_fp8_kernel<false, true><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                       err_flag, S);
     else
-        combine_fp8_kernel<false><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows, err_flag);
+        combine_fp8_kernel<false, false><<<grid, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                        err_flag, 1);
     return cudaGetLastError();
 }
 
