@@ -287,6 +287,95 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
     }
 }
 
+// Few slots per token (k <= 2, Mixtral-like routing): one warp per token and
+// no block barrier.  A CTA-per-token combine keeps only k loads in flight
+// per thread there and waits at two barriers per token; here each lane
+// takes kWarpChunks 16-byte column chunks of the row at once (k * kWarpChunks
+// loads in flight), and warps move to their next token independently, its
+// rows and weights fetched while the current one is summed.  Each column's
+// fma chain is the one combine_kernel runs.
+constexpr int kWarpChunks = 4;
+
+__global__ void __launch_bounds__(kCombThreads) combine_warp_kernel(const uint16_t *__restrict__ y,
+                                                                    const int32_t *__restrict__ pos,
+                                                                    const float *__restrict__ w, int T, int H, int k,
+                                                                    uint16_t *__restrict__ out, long long rows,
+                                                                    int32_t *__restrict__ err_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int C = H / 8;
+    // lane j < k holds slot j's row and weight (k <= 2)
+    int np = -1;
+    float nw = 0.0f;
+    if (warp < T && lane < k) {
+        np = __ldg(pos + warp * k + lane);
+        nw = w ? __ldg(w + warp * k + lane) : 1.0f;
+    }
+    for (long long t = warp; t < T; t += nwarps) {
+        int p = np;
+        if (lane < k && p >= rows) {
+            if (err_flag)
+                atomicOr(err_flag, 2);
+            p = -1;
+        }
+        const int p0 = __shfl_sync(kFullMask, p, 0), p1 = __shfl_sync(kFullMask, p, 1);
+        const float w0 = __shfl_sync(kFullMask, nw, 0), w1 = __shfl_sync(kFullMask, nw, 1);
+        const int q0 = k > 0 ? p0 : -1, q1 = k > 1 ? p1 : -1;
+        const long long tn = t + nwarps;  // the next token's rows and weights
+        if (tn < T && lane < k) {
+            np = __ldg(pos + tn * k + lane);
+            nw = w ? __ldg(w + tn * k + lane) : 1.0f;
+        }
+        for (int c0 = lane; c0 < C; c0 += 32 * kWarpChunks) {
+            uint4 v0[kWarpChunks], v1[kWarpChunks];
+#pragma unroll
+            for (int m = 0; m < kWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c < C) {
+                    if (q0 >= 0)
+                        v0[m] = ld_stream16(y + (size_t)q0 * H + (size_t)c * 8);
+                    if (q1 >= 0)
+                        v1[m] = ld_stream16(y + (size_t)q1 * H + (size_t)c * 8);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c >= C)
+                    continue;
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = 0.0f;
+                if (q0 >= 0) {
+                    const uint32_t vv[4] = {v0[m].x, v0[m].y, v0[m].z, v0[m].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = fmaf(w0, bf16_lo(vv[i]), acc[2 * i]);
+                        acc[2 * i + 1] = fmaf(w0, bf16_hi(vv[i]), acc[2 * i + 1]);
+                    }
+                }
+                if (q1 >= 0) {
+                    const uint32_t vv[4] = {v1[m].x, v1[m].y, v1[m].z, v1[m].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = fmaf(w1, bf16_lo(vv[i]), acc[2 * i]);
+                        acc[2 * i + 1] = fmaf(w1, bf16_hi(vv[i]), acc[2 * i + 1]);
+                    }
+                }
+                uint4 o;
+                o.x = pack_bf16x2(acc[0], acc[1]);
+                o.y = pack_bf16x2(acc[2], acc[3]);
+                o.z = pack_bf16x2(acc[4], acc[5]);
+                o.w = pack_bf16x2(acc[6], acc[7]);
+                st_stream16(out + (size_t)t * H + (size_t)c * 8, o);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos, const float *w, int T, int H,
@@ -294,6 +383,20 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 2 && T >= 2048) {
+        static int wps = 0;
+        if (wps < 1) {
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&wps, (const void *)combine_warp_kernel, kCombThreads, 0);
+            if (wps < 1)
+                wps = 1;
+        }
+        const long long need = ((long long)T + kCombThreads / 32 - 1) / (kCombThreads / 32);
+        long long g = (long long)device_sm_count() * wps;
+        if (g > need)
+            g = need;
+        combine_warp_kernel<<<(int)g, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag);
+        return cudaGetLastError();
+    }
     static int per_sm = 0;  // the same registers either way: sized on the unsplit kernel
     if (per_sm < 1) {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_kernel<false>, kCombThreads, 0);

@@ -65,7 +65,8 @@ def test_combine_full_size_arbitrary_outputs(ep, name):
     _combine_both(ep, y, pos, w)
 
 
-@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (5, 16, 3), (33, 264, 8), (64, 7168, 9), (300, 512, 17), (7, 64, 40), (5, 16384, 64)])
+@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (5, 16, 3), (33, 264, 8), (64, 7168, 9), (300, 512, 17), (7, 64, 40), (5, 16384, 64),
+                                   (2100, 64, 1), (2500, 1032, 2)])   # the last two: one warp per token
 def test_combine_small_shapes_signed_weights_empty_slots(ep, T, H, k):
     rng = np.random.default_rng(T + H + k)
     y = synth.f32_to_bf16_bits(rng.normal(0, 1, (T * k, H)).astype(np.float32))
