@@ -376,6 +376,111 @@ __global__ void __launch_bounds__(kCombThreads) combine_warp_kernel(const uint16
     }
 }
 
+// The FP8 / MXFP8-input combine with one warp per token for k <= 2, as
+// combine_warp_kernel: each lane takes kWarpChunks 16-column chunks at once
+// (16 codes and their block scale per slot); the arithmetic is
+// combine_fp8_kernel's (w * s once per slot and block, then the fma chain).
+template <bool kMx>
+__global__ void __launch_bounds__(kCombThreads) combine_fp8_warp_kernel(const uint8_t *__restrict__ yq,
+                                                                        const void *__restrict__ yscale,
+                                                                        const int32_t *__restrict__ pos,
+                                                                        const float *__restrict__ w, int T, int H,
+                                                                        int k, uint16_t *__restrict__ out,
+                                                                        long long rows,
+                                                                        int32_t *__restrict__ err_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int C16 = H / 16;
+    const int nb = kMx ? H / 32 : H / 128;
+    int np = -1;
+    float nw = 0.0f;
+    if (warp < T && lane < k) {
+        np = __ldg(pos + warp * k + lane);
+        nw = __ldg(w + warp * k + lane);
+    }
+    for (long long t = warp; t < T; t += nwarps) {
+        int p = np;
+        if (lane < k && p >= rows) {
+            if (err_flag)
+                atomicOr(err_flag, 2);
+            p = -1;
+        }
+        const int p0 = __shfl_sync(kFullMask, p, 0), p1 = __shfl_sync(kFullMask, p, 1);
+        const float w0 = __shfl_sync(kFullMask, nw, 0), w1 = __shfl_sync(kFullMask, nw, 1);
+        const int q0 = k > 0 ? p0 : -1, q1 = k > 1 ? p1 : -1;
+        const long long tn = t + nwarps;
+        if (tn < T && lane < k) {
+            np = __ldg(pos + tn * k + lane);
+            nw = __ldg(w + tn * k + lane);
+        }
+        for (int c0 = lane; c0 < C16; c0 += 32 * kWarpChunks) {
+            uint4 v0[kWarpChunks], v1[kWarpChunks];
+            uint32_t s0[kWarpChunks], s1[kWarpChunks];
+#pragma unroll
+            for (int m = 0; m < kWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c >= C16)
+                    continue;
+                const int sb = kMx ? (c >> 1) : (c >> 3);
+                if (q0 >= 0) {
+                    v0[m] = ld_stream16(yq + (size_t)q0 * H + (size_t)c * 16);
+                    s0[m] = kMx ? (uint32_t)__ldg(static_cast<const uint8_t *>(yscale) + (size_t)q0 * nb + sb)
+                                : __float_as_uint(__ldg(static_cast<const float *>(yscale) + (size_t)q0 * nb + sb));
+                }
+                if (q1 >= 0) {
+                    v1[m] = ld_stream16(yq + (size_t)q1 * H + (size_t)c * 16);
+                    s1[m] = kMx ? (uint32_t)__ldg(static_cast<const uint8_t *>(yscale) + (size_t)q1 * nb + sb)
+                                : __float_as_uint(__ldg(static_cast<const float *>(yscale) + (size_t)q1 * nb + sb));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c >= C16)
+                    continue;
+                float acc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    acc[i] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int q = j == 0 ? q0 : q1;
+                    if (q < 0)
+                        continue;
+                    const uint32_t sr = j == 0 ? s0[m] : s1[m];
+                    const float sc = kMx ? e8m0_to_f32(sr) : __uint_as_float(sr);
+                    const float ws = (j == 0 ? w0 : w1) * sc;
+                    const uint4 v = j == 0 ? v0[m] : v1[m];
+                    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float d0, d1, d2, d3;
+                        e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
+                        acc[4 * i] = fmaf(ws, d0, acc[4 * i]);
+                        acc[4 * i + 1] = fmaf(ws, d1, acc[4 * i + 1]);
+                        acc[4 * i + 2] = fmaf(ws, d2, acc[4 * i + 2]);
+                        acc[4 * i + 3] = fmaf(ws, d3, acc[4 * i + 3]);
+                    }
+                }
+                uint4 o0, o1;
+                o0.x = pack_bf16x2(acc[0], acc[1]);
+                o0.y = pack_bf16x2(acc[2], acc[3]);
+                o0.z = pack_bf16x2(acc[4], acc[5]);
+                o0.w = pack_bf16x2(acc[6], acc[7]);
+                o1.x = pack_bf16x2(acc[8], acc[9]);
+                o1.y = pack_bf16x2(acc[10], acc[11]);
+                o1.z = pack_bf16x2(acc[12], acc[13]);
+                o1.w = pack_bf16x2(acc[14], acc[15]);
+                uint16_t *dst = out + (size_t)t * H + (size_t)c * 16;
+                st_stream16(dst, o0);
+                st_stream16(dst + 8, o1);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos, const float *w, int T, int H,
@@ -423,6 +528,27 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 2 && T >= 2048) {
+        static int wps[2] = {0, 0};
+        const void *wk = mx ? (const void *)combine_fp8_warp_kernel<true> : (const void *)combine_fp8_warp_kernel<false>;
+        int &ps = wps[mx ? 1 : 0];
+        if (ps < 1) {
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, wk, kCombThreads, 0);
+            if (ps < 1)
+                ps = 1;
+        }
+        const long long need = ((long long)T + kCombThreads / 32 - 1) / (kCombThreads / 32);
+        long long g = (long long)device_sm_count() * ps;
+        if (g > need)
+            g = need;
+        if (mx)
+            combine_fp8_warp_kernel<true><<<(int)g, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                          err_flag);
+        else
+            combine_fp8_warp_kernel<false><<<(int)g, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+                                                                           err_flag);
+        return cudaGetLastError();
+    }
     static int per_sm_cache[2] = {0, 0};
     const void *kern =
         mx ? (const void *)combine_fp8_kernel<true, false> : (const void *)combine_fp8_kernel<false, false>;

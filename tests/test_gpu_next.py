@@ -90,7 +90,8 @@ def _dequant(q, s, bs):
     return vals * np.repeat(scale, bs, axis=1)
 
 
-@pytest.mark.parametrize("name,fmt", [("dsv3", "fp8"), ("dsv3", "mxfp8"), ("decode", "fp8"), ("qwen3", "mxfp8")])
+@pytest.mark.parametrize("name,fmt", [("dsv3", "fp8"), ("dsv3", "mxfp8"), ("decode", "fp8"), ("qwen3", "mxfp8"),
+                                      ("mixtral", "fp8"), ("mixtral", "mxfp8")])
 def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     cfg = synth.config(name)
     inp = synth.make_inputs(cfg)
@@ -110,6 +111,8 @@ def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     # bytes); a scale buffer 4 bytes off a 16-byte boundary
     ("fp8", 2048, 1024, 6, 0), ("mxfp8", 2100, 512, 8, 0), ("fp8", 2048, 384, 4, 0), ("mxfp8", 2049, 96, 5, 0),
     ("fp8", 2048, 1024, 6, 4),
+    # k <= 2 on large batches: one warp per token
+    ("fp8", 2048, 1024, 2, 0), ("mxfp8", 2100, 96, 1, 0), ("fp8", 2500, 384, 2, 4),
 ])
 def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset):
     rng = np.random.default_rng(9 + T + H)
