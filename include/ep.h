@@ -295,7 +295,10 @@ ep_status ep_combine_fp8(const void *yq, const void *yscales, int32_t scale_dtyp
  * tokens with a kept entry on the rank; expert_dropped[E] = entries past
  * capacity; src has E*capacity rows (-1 for an empty row).  The receive
  * buffer needs E*capacity rows.  workspace as ep_get_layout.  Limits as
- * ep_get_layout and E*capacity < 2^31.
+ * ep_get_layout and E*capacity < 2^31.  Like ep_get_layout's larger
+ * batches, this runs as one cooperative launch with a bounded grid barrier
+ * (EP_FLAG_TIMEOUT if its wait runs out) unless one CTA per SM would hold
+ * more than 4096 entries, then as three launches.
  */
 ep_status ep_get_layout_capacity(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E,
                                  int32_t experts_per_rank, int32_t capacity, int32_t *expert_count,
