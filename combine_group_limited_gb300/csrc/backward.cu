@@ -166,6 +166,124 @@ __global__ void __launch_bounds__(kBwdThreads, 3) combine_backward_kernel(
     }
 }
 
+// grad_y of one 16-byte chunk for one slot: the 8 products w * g rounded
+// once to bf16 (midpoints among them take the exact path, as in
+// combine_backward_kernel), and the slot's dot product advanced by the chunk.
+__device__ __forceinline__ uint4 backward_chunk(float wj, const float (&g)[8], const uint4 &yv4, float &dot)
+{
+    const uint32_t yv[4] = {yv4.x, yv4.y, yv4.z, yv4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dot = fmaf(g[2 * i], bf16_lo(yv[i]), dot);
+        dot = fmaf(g[2 * i + 1], bf16_hi(yv[i]), dot);
+    }
+    float pr[8];
+    uint32_t mid = 0xFFFFu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        pr[i] = wj * g[i];
+        mid = min(mid, (__float_as_uint(pr[i]) & 0xFFFFu) ^ 0x8000u);
+    }
+    if (mid == 0u) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            pr[i] = exact_product_for_bf16(wj, g[i]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(pr[0], pr[1]);
+    o.y = pack_bf16x2(pr[2], pr[3]);
+    o.z = pack_bf16x2(pr[4], pr[5]);
+    o.w = pack_bf16x2(pr[6], pr[7]);
+    return o;
+}
+
+// k <= 2 on large batches: one warp per token and no block barriers.  A
+// CTA-per-token pass pays a memory round trip and four barriers per token,
+// which at two slots is most of the token's time.  Each lane takes
+// kBwdWarpChunks 16-byte chunks at once (grad_out and both slots' rows
+// loaded before any arithmetic), and the next token's rows and weights are
+// fetched while one is processed.  Each lane's dots run over its chunks in
+// order and are then summed by a warp xor-tree: a fixed order, so grad_w
+// does not depend on timing.  Blocks of 4 warps at up to 64 registers keep
+// 32 warps on an SM.
+constexpr int kBwdWarpThreads = 128;
+constexpr int kBwdWarpChunks = 2;
+
+__global__ void __launch_bounds__(kBwdWarpThreads, 8) combine_backward_warp_kernel(
+    const uint16_t *__restrict__ grad_out, const uint16_t *__restrict__ y, const int32_t *__restrict__ pos,
+    const float *__restrict__ w, int T, int H, int k, uint16_t *__restrict__ grad_y, float *__restrict__ grad_w,
+    long long rows, int32_t *__restrict__ err_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);  // grid <= T/4 + 1 blocks
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int C = H / 8;
+    int np = -1;
+    float nw = 0.0f;
+    if (warp < T && lane < k) {
+        np = __ldg(pos + (size_t)warp * k + lane);
+        nw = __ldg(w + (size_t)warp * k + lane);
+    }
+    for (int t = warp; t < T; t += nwarps) {
+        int p = np;
+        if (lane < k && p >= rows) {
+            if (err_flag)
+                atomicOr(err_flag, 2);
+            p = -1;
+        }
+        const int p0 = __shfl_sync(kFullMask, p, 0), p1 = __shfl_sync(kFullMask, p, 1);
+        const float w0 = __shfl_sync(kFullMask, nw, 0), w1 = __shfl_sync(kFullMask, nw, 1);
+        const int q1 = k > 1 ? p1 : -1;
+        const int tn = t + nwarps;  // < 2T: no overflow
+        if (tn < T && lane < k) {
+            np = __ldg(pos + (size_t)tn * k + lane);
+            nw = __ldg(w + (size_t)tn * k + lane);
+        }
+        const uint16_t *grow = grad_out + (size_t)t * H;
+        float d0 = 0.0f, d1 = 0.0f;
+        for (int c0 = lane; c0 < C; c0 += 32 * kBwdWarpChunks) {
+            uint4 gv[kBwdWarpChunks], v0[kBwdWarpChunks], v1[kBwdWarpChunks];
+#pragma unroll
+            for (int m = 0; m < kBwdWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c >= C)
+                    continue;
+                gv[m] = ld_stream16(grow + (size_t)c * 8);
+                if (p0 >= 0)
+                    v0[m] = ld_stream16(y + (size_t)p0 * H + (size_t)c * 8);
+                if (q1 >= 0)
+                    v1[m] = ld_stream16(y + (size_t)q1 * H + (size_t)c * 8);
+            }
+#pragma unroll
+            for (int m = 0; m < kBwdWarpChunks; ++m) {
+                const int c = c0 + 32 * m;
+                if (c >= C)
+                    continue;
+                const uint32_t gw4[4] = {gv[m].x, gv[m].y, gv[m].z, gv[m].w};
+                float g[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    g[2 * i] = bf16_lo(gw4[i]);
+                    g[2 * i + 1] = bf16_hi(gw4[i]);
+                }
+                if (p0 >= 0)
+                    st_plain16(grad_y + (size_t)p0 * H + (size_t)c * 8, backward_chunk(w0, g, v0[m], d0));
+                if (q1 >= 0)
+                    st_plain16(grad_y + (size_t)q1 * H + (size_t)c * 8, backward_chunk(w1, g, v1[m], d1));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            d0 += __shfl_xor_sync(kFullMask, d0, off);
+            d1 += __shfl_xor_sync(kFullMask, d1, off);
+        }
+        if (lane == 0)
+            grad_w[(size_t)t * k] = p0 >= 0 ? d0 : 0.0f;
+        if (lane == 1 && k > 1)
+            grad_w[(size_t)t * k + 1] = q1 >= 0 ? d1 : 0.0f;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y, long long rows, const int32_t *pos,
@@ -174,6 +292,22 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 2 && T >= 2048) {
+        static int per_sm = 0;
+        if (per_sm < 1) {
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_backward_warp_kernel,
+                                                          kBwdWarpThreads, 0);
+            if (per_sm < 1)
+                per_sm = 1;
+        }
+        const long long need = ((long long)T + kBwdWarpThreads / 32 - 1) / (kBwdWarpThreads / 32);
+        long long g = (long long)device_sm_count() * per_sm;
+        if (g > need)
+            g = need;
+        combine_backward_warp_kernel<<<(int)g, kBwdWarpThreads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y,
+                                                                          grad_w, rows, err_flag);
+        return cudaGetLastError();
+    }
     const int threads = chunk_threads(H / 8, k);  // <= kBwdThreads (k <= 64)
     static int cached_threads = 0, cached_per_sm = 0;
     const int grid = row_grid((const void *)combine_backward_kernel, threads, T, cached_threads, cached_per_sm);

@@ -376,12 +376,16 @@ __global__ void __launch_bounds__(kCombThreads) combine_warp_kernel(const uint16
     }
 }
 
+// Blocks of 4 warps at up to 72 registers a thread keep 28 warps on an SM
+// (7 blocks), so a 4096-token batch finishes in one round of warps.
+constexpr int kFp8WarpThreads = 128;
+
 // The FP8 / MXFP8-input combine with one warp per token for k <= 2, as
 // combine_warp_kernel: each lane takes kWarpChunks 16-column chunks at once
 // (16 codes and their block scale per slot); the arithmetic is
 // combine_fp8_kernel's (w * s once per slot and block, then the fma chain).
 template <bool kMx>
-__global__ void __launch_bounds__(kCombThreads) combine_fp8_warp_kernel(const uint8_t *__restrict__ yq,
+__global__ void __launch_bounds__(kFp8WarpThreads, 7) combine_fp8_warp_kernel(const uint8_t *__restrict__ yq,
                                                                         const void *__restrict__ yscale,
                                                                         const int32_t *__restrict__ pos,
                                                                         const float *__restrict__ w, int T, int H,
@@ -533,19 +537,19 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
         const void *wk = mx ? (const void *)combine_fp8_warp_kernel<true> : (const void *)combine_fp8_warp_kernel<false>;
         int &ps = wps[mx ? 1 : 0];
         if (ps < 1) {
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, wk, kCombThreads, 0);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, wk, kFp8WarpThreads, 0);
             if (ps < 1)
                 ps = 1;
         }
-        const long long need = ((long long)T + kCombThreads / 32 - 1) / (kCombThreads / 32);
+        const long long need = ((long long)T + kFp8WarpThreads / 32 - 1) / (kFp8WarpThreads / 32);
         long long g = (long long)device_sm_count() * ps;
         if (g > need)
             g = need;
         if (mx)
-            combine_fp8_warp_kernel<true><<<(int)g, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+            combine_fp8_warp_kernel<true><<<(int)g, kFp8WarpThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
                                                                           err_flag);
         else
-            combine_fp8_warp_kernel<false><<<(int)g, kCombThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
+            combine_fp8_warp_kernel<false><<<(int)g, kFp8WarpThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
                                                                            err_flag);
         return cudaGetLastError();
     }

@@ -184,11 +184,12 @@ ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, cons
         return EP_ERR_ALIGNMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ep::GateParams gp = gate_params(cfg);
-    if (T > 0 && ep::route_supported(T, k, E))
+    if ((long long)T * k > ep::kSmallLayoutEntries && ep::route_supported(T, k, E))
         return launched(ep::launch_route(scores, bias, &gp, nullptr, topk_idx, topk_w, T, k, E, experts_per_rank,
                                          expert_count, expert_off, rank_count, rank_off, rank_tokens, pos, src,
                                          err_flag, workspace, st));
-    // batches the single launch does not cover: the two steps' own kernels
+    // one-CTA layouts and batches too large for the single launch: the two
+    // steps' own kernels
     cudaError_t e = ep::launch_gate(scores, bias, T, gp, topk_idx, topk_w, st);
     if (e == cudaSuccess)
         e = ep::launch_layout(topk_idx, T, k, E, experts_per_rank, expert_count, expert_off, rank_count, rank_off,

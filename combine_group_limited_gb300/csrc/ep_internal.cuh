@@ -159,6 +159,9 @@ cudaError_t launch_barrier_selftest(unsigned extra, long long spin_limit, int32_
 // barrier's arrival count) zero, and left zero by every call that completes.
 size_t route_workspace_bytes(int E);
 bool route_supported(int T, int k, int E);
+
+// Layouts of at most this many entries (T*k) run as one kernel on one CTA.
+constexpr int kSmallLayoutEntries = 4096;
 cudaError_t launch_route(const float *scores, const float *bias, const GateParams *gp, const int32_t *topk_idx_in,
                          int32_t *topk_idx, float *topk_w, int T, int k, int E, int epr, int32_t *expert_count,
                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,

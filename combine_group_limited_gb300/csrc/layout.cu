@@ -40,7 +40,7 @@ constexpr int kPlaceWarps = kPlaceThreads / 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kSmallThreads = 512;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallEntries = 4096;  // single-launch layout up to this many entries
+constexpr int kSmallEntries = kSmallLayoutEntries;
 constexpr int kSmallChunks = kSmallEntries / (kSmallWarps * 32);  // 32-entry chunks per warp
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return (unsigned)e < (unsigned)E; }

@@ -163,7 +163,9 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
  * batch size; here, while a grid of one CTA per SM covers the batch with at
  * most 4096 entries per CTA, both run in one cooperative launch whose CTAs
  * gate and count their own tokens, meet at one grid barrier and then place
- * them.  Larger batches run the two calls' own kernels.
+ * them.  Batches of at most 4096 entries (T*k), where one CTA lays out the
+ * whole batch and a grid-wide launch only adds latency, and batches too large
+ * for that grid run the two calls' own kernels.
  *
  * Arguments: those of ep_gate (scores, bias, T, cfg, topk_idx, topk_w) and
  * of ep_get_layout (experts_per_rank, expert_count .. src, err_flag), with

@@ -275,3 +275,35 @@ def test_combine_backward_empty_slots_and_midpoints(ep):
     _, ogw = oracle.combine_backward(g, y, pos, w, grad_y=ref_gy)
     np.testing.assert_array_equal(host_bits(gy), ref_gy)
     assert np.all(gw.cpu().numpy()[pos < 0] == 0)
+
+
+@pytest.mark.parametrize("T,H,k", [(2048, 256, 1), (2100, 1032, 2), (2500, 136, 2), (3001, 4096, 1)])
+def test_combine_backward_warp_per_token(ep, T, H, k):
+    """k <= 2 on 2048+ tokens (one warp per token): ragged rows (H/8 not a
+    multiple of the warp's chunk step), empty slots, and products next to
+    bf16 midpoints; grad_y bit exact, untouched rows left alone, grad_w 0 on
+    empty slots and within the fp32 dot-product bound elsewhere."""
+    rng = np.random.default_rng(T + H + k)
+    rows = T * k + 7
+    w = np.full((T, k), 1 + 2.0 ** -8 + 2.0 ** -20, np.float32)
+    w[::3] = 1 + 2.0 ** -8 - 2.0 ** -20
+    w[1::3] = rng.random((len(w[1::3]), k)).astype(np.float32)
+    g = synth.f32_to_bf16_bits(rng.normal(0, 1, (T, H)).astype(np.float32))
+    y = synth.f32_to_bf16_bits(rng.normal(0, 1, (rows, H)).astype(np.float32))
+    pos = rng.permutation(rows)[:T * k].reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.1] = -1
+    gy_d = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gy, gw = ep.ep_combine_backward(dev_bf16(g), dev_bf16(y), dev(pos), dev(w), grad_y=gy_d, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    ref_gy = np.full((rows, H), 0x4040, np.uint16)
+    _, ogw = oracle.combine_backward(g, y, pos, w, grad_y=ref_gy)
+    np.testing.assert_array_equal(host_bits(gy), ref_gy)
+    gwn = gw.cpu().numpy()
+    assert np.all(gwn[pos < 0] == 0)
+    gf = synth.bf16_bits_to_f32(g).astype(np.float64)
+    yf = synth.bf16_bits_to_f32(y).astype(np.float64)
+    S = np.einsum("th,tkh->tk", np.abs(gf), np.abs(yf[np.maximum(pos, 0)]))
+    ok = pos >= 0
+    assert np.all(np.abs(gwn - ogw)[ok] <= H * U * S[ok] + 1e-30)

@@ -1,8 +1,9 @@
-"""GPU parity of the single-launch routing: ep_gate_layout (gating and layout
-in one cooperative launch) and ep_get_layout's cooperative path for batches
-of more than 4096 entries, against the CPU oracle and against the separate
-calls; the grid barrier's bounded wait reports a workspace whose barrier
-words are not clear."""
+"""GPU parity of the routing call ep_gate_layout (gating and layout in one
+cooperative launch above 4096 entries, the gate kernel and the one-CTA
+layout below) and of ep_get_layout's cooperative path for batches of more
+than 4096 entries, against the CPU oracle and against the separate calls;
+the grid barrier's bounded wait reports a workspace whose barrier words are
+not clear."""
 import numpy as np
 import pytest
 import torch
