@@ -30,16 +30,43 @@ namespace {
 
 constexpr int kDispThreads = 256;
 
+// The item kernels are software-pipelined: a warp issues the next item's
+// row and pos loads before it checks, converts and stores the current one,
+// so the check of pos (a branch on a loaded value, which stalls in-order
+// issue) and the row loads of one item never form two round trips in a row.
 __global__ void __launch_bounds__(kDispThreads) dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                                      int k, const int32_t *__restrict__ pos,
                                                                      uint16_t *__restrict__ recv, long long rows,
                                                                      int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    for (ItemWalk it(T, bf16_segs(H)); it.valid(); it.next()) {
-        int p0, p1;
-        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        dispatch_bf16_item(x, H, k, it.t, it.seg, p0, p1, recv);
+    ItemWalk it(T, bf16_segs(H));
+    if (!it.valid())
+        return;
+    int p0, p1;
+    uint4 v[kBf16Unroll];
+    load_token_rows(pos, it.t, k, lane, p0, p1);
+    bf16_item_load(x, H, it.t, it.seg, v);
+    for (;;) {
+        ItemWalk nx = it;
+        nx.next();
+        const bool more = nx.valid();  // warp-uniform
+        int n0 = -1, n1 = -1;
+        uint4 nv[kBf16Unroll];
+        if (more) {
+            load_token_rows(pos, nx.t, k, lane, n0, n1);
+            bf16_item_load(x, H, nx.t, nx.seg, nv);
+        }
+        check_token_rows(rows, err_flag, p0, p1);
+        bf16_item_store(H, k, it.seg, p0, p1, v, recv);
+        if (!more)
+            break;
+        it = nx;
+        p0 = n0;
+        p1 = n1;
+#pragma unroll
+        for (int u = 0; u < kBf16Unroll; ++u)
+            v[u] = nv[u];
     }
 }
 
@@ -50,10 +77,32 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16
                                                                     int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    for (ItemWalk it(T, fp8_segs(H)); it.valid(); it.next()) {
-        int p0, p1;
-        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        dispatch_fp8_item(x, H, k, it.t, it.seg, p0, p1, recv_q, recv_s);
+    ItemWalk it(T, fp8_segs(H));
+    if (!it.valid())
+        return;
+    int p0, p1;
+    uint4 a, b;
+    load_token_rows(pos, it.t, k, lane, p0, p1);
+    q8_item_load(x, H, it.t, it.seg, a, b);
+    for (;;) {
+        ItemWalk nx = it;
+        nx.next();
+        const bool more = nx.valid();  // warp-uniform
+        int n0 = -1, n1 = -1;
+        uint4 na = make_uint4(0, 0, 0, 0), nb = make_uint4(0, 0, 0, 0);
+        if (more) {
+            load_token_rows(pos, nx.t, k, lane, n0, n1);
+            q8_item_load(x, H, nx.t, nx.seg, na, nb);
+        }
+        check_token_rows(rows, err_flag, p0, p1);
+        fp8_item_store(H, k, it.seg, p0, p1, a, b, recv_q, recv_s);
+        if (!more)
+            break;
+        it = nx;
+        p0 = n0;
+        p1 = n1;
+        a = na;
+        b = nb;
     }
 }
 
@@ -70,10 +119,32 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_mxfp8_kernel(const uint
                                                                       int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    for (ItemWalk it(T, fp8_segs(H)); it.valid(); it.next()) {
-        int p0, p1;
-        token_rows(pos, it.t, k, rows, lane, err_flag, p0, p1);
-        dispatch_mxfp8_item(x, H, k, it.t, it.seg, p0, p1, recv_q, recv_e);
+    ItemWalk it(T, fp8_segs(H));
+    if (!it.valid())
+        return;
+    int p0, p1;
+    uint4 a, b;
+    load_token_rows(pos, it.t, k, lane, p0, p1);
+    q8_item_load(x, H, it.t, it.seg, a, b);
+    for (;;) {
+        ItemWalk nx = it;
+        nx.next();
+        const bool more = nx.valid();  // warp-uniform
+        int n0 = -1, n1 = -1;
+        uint4 na = make_uint4(0, 0, 0, 0), nb = make_uint4(0, 0, 0, 0);
+        if (more) {
+            load_token_rows(pos, nx.t, k, lane, n0, n1);
+            q8_item_load(x, H, nx.t, nx.seg, na, nb);
+        }
+        check_token_rows(rows, err_flag, p0, p1);
+        mxfp8_item_store(H, k, it.seg, p0, p1, a, b, recv_q, recv_e);
+        if (!more)
+            break;
+        it = nx;
+        p0 = n0;
+        p1 = n1;
+        a = na;
+        b = nb;
     }
 }
 

@@ -17,8 +17,8 @@ constexpr int kBf16Unroll = 4;  // 16-byte chunks per lane per item (BF16)
 // Receive rows of token t for the calling warp: slot `lane` in p0, slot
 // `lane + 32` in p1; -1 where the slot does not exist, is empty, or names a
 // row outside [0, rows) (flagged).
-__device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long long t, int k, long long rows,
-                                           int lane, int32_t *err_flag, int &p0, int &p1)
+__device__ __forceinline__ void load_token_rows(const int32_t *__restrict__ pos, long long t, int k, int lane, int &p0,
+                                                int &p1)
 {
     p0 = -1;
     p1 = -1;
@@ -26,6 +26,10 @@ __device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long
         p0 = __ldg(pos + t * k + lane);
     if (lane + 32 < k)
         p1 = __ldg(pos + t * k + lane + 32);
+}
+
+__device__ __forceinline__ void check_token_rows(long long rows, int32_t *err_flag, int &p0, int &p1)
+{
     if (p0 >= rows || p1 >= rows) {
         if (err_flag)
             atomicOr(err_flag, 2);
@@ -36,6 +40,13 @@ __device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long
     }
 }
 
+__device__ __forceinline__ void token_rows(const int32_t *__restrict__ pos, long long t, int k, long long rows,
+                                           int lane, int32_t *err_flag, int &p0, int &p1)
+{
+    load_token_rows(pos, t, k, lane, p0, p1);
+    check_token_rows(rows, err_flag, p0, p1);
+}
+
 __device__ __forceinline__ int slot_row(int p0, int p1, int j)
 {
     const int a = __shfl_sync(kFullMask, p0, j & 31);
@@ -44,11 +55,6 @@ __device__ __forceinline__ int slot_row(int p0, int p1, int j)
 }
 
 // Walks warp items (token, segment) grid-stride without a division per item.
-struct ItemPos {
-    long long t;
-    int seg;
-};
-
 struct ItemWalk {
     long long t;
     int seg;
@@ -84,22 +90,29 @@ struct ItemWalk {
 __device__ __host__ __forceinline__ int bf16_segs(int H) { return (H / 8 + 32 * kBf16Unroll - 1) / (32 * kBf16Unroll); }
 __device__ __host__ __forceinline__ int fp8_segs(int H) { return (H / 16 + 31) / 32; }
 
-// BF16: recv[p_j, seg] = x[t, seg] for the token's k rows.
-__device__ __forceinline__ void dispatch_bf16_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
-                                                   int p0, int p1, uint16_t *__restrict__ recv)
+// BF16: recv[p_j, seg] = x[t, seg] for the token's k rows.  The load half
+// and the store half are separate so that a kernel can issue the next item's
+// loads before storing this one.
+__device__ __forceinline__ void bf16_item_load(const uint16_t *__restrict__ x, int H, long long t, int seg,
+                                               uint4 (&v)[kBf16Unroll])
 {
     const int lane = threadIdx.x & 31;
     const int C = H / 8;  // 16-byte chunks per row
-    ItemPos it{t, seg};
-    const uint16_t *xrow = x + (size_t)it.t * H;
-    const int c0 = it.seg * 32 * kBf16Unroll + lane;
-    uint4 v[kBf16Unroll];
+    const uint16_t *xrow = x + (size_t)t * H;
+    const int c0 = seg * 32 * kBf16Unroll + lane;
 #pragma unroll
     for (int u = 0; u < kBf16Unroll; ++u) {
         const int c = c0 + 32 * u;
-        if (c < C)
-            v[u] = ld_stream16(xrow + (size_t)c * 8);
+        v[u] = c < C ? ld_stream16(xrow + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ void bf16_item_store(int H, int k, int seg, int p0, int p1, const uint4 (&v)[kBf16Unroll],
+                                                uint16_t *__restrict__ recv)
+{
+    const int lane = threadIdx.x & 31;
+    const int C = H / 8;
+    const int c0 = seg * 32 * kBf16Unroll + lane;
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0)
@@ -114,17 +127,33 @@ __device__ __forceinline__ void dispatch_bf16_item(const uint16_t *__restrict__ 
     }
 }
 
+__device__ __forceinline__ void dispatch_bf16_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
+                                                   int p0, int p1, uint16_t *__restrict__ recv)
+{
+    uint4 v[kBf16Unroll];
+    bf16_item_load(x, H, t, seg, v);
+    bf16_item_store(H, k, seg, p0, p1, v, recv);
+}
+
 // FP8 e4m3 with one fp32 scale per 128 columns: the codes of the 16 columns
 // [16c, 16c + 16) of row xrow and their block's scale s = amax / 448.  Eight
 // consecutive lanes cover a block: every lane of the warp calls this (lanes
 // with act == false contribute zeros).
-__device__ __forceinline__ uint4 fp8_quant16(const uint16_t *__restrict__ xrow, int c, bool act, float &s_out)
+// The 16 bf16 values [16c, 16c + 16) of row xrow as two 16-byte words
+// (zeros where act is false).
+__device__ __forceinline__ void load16(const uint16_t *__restrict__ xrow, int c, bool act, uint4 &a, uint4 &b)
 {
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    a = make_uint4(0, 0, 0, 0);
+    b = make_uint4(0, 0, 0, 0);
     if (act) {
         a = ld_stream16(xrow + (size_t)c * 16);
         b = ld_stream16(xrow + (size_t)c * 16 + 8);
     }
+}
+
+// fp8_quant16's arithmetic on 16 values already loaded by load16.
+__device__ __forceinline__ uint4 fp8_quant16_regs(const uint4 &a, const uint4 &b, float &s_out)
+{
     const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float f[16];
 #pragma unroll
@@ -161,21 +190,34 @@ __device__ __forceinline__ uint4 fp8_quant16(const uint16_t *__restrict__ xrow, 
     return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.
-__device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
-                                                  int p0, int p1, uint8_t *__restrict__ recv_q,
-                                                  float *__restrict__ recv_s)
+__device__ __forceinline__ uint4 fp8_quant16(const uint16_t *__restrict__ xrow, int c, bool act, float &s_out)
+{
+    uint4 a, b;
+    load16(xrow, c, act, a, b);
+    return fp8_quant16_regs(a, b, s_out);
+}
+
+// The 16 columns a lane owns in item (t, seg) of an FP8 / MXFP8 dispatch.
+__device__ __forceinline__ void q8_item_load(const uint16_t *__restrict__ x, int H, long long t, int seg, uint4 &a,
+                                             uint4 &b)
+{
+    const int c = seg * 32 + (threadIdx.x & 31);
+    load16(x + (size_t)t * H, c, c < H / 16, a, b);
+}
+
+// FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.  The
+// store half takes the item's values from q8_item_load.
+__device__ __forceinline__ void fp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a, const uint4 &b,
+                                               uint8_t *__restrict__ recv_q, float *__restrict__ recv_s)
 {
     const int lane = threadIdx.x & 31;
     const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
     const int nb = H / 128;  // scales per row
-    ItemPos it{t, seg};
-    const uint16_t *xrow = x + (size_t)it.t * H;
-    const int c = it.seg * 32 + lane;
+    const int c = seg * 32 + lane;
     // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
     const bool act = c < C16;
     float s;
-    const uint4 qv = fp8_quant16(xrow, c, act, s);
+    const uint4 qv = fp8_quant16_regs(a, b, s);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)
@@ -186,16 +228,20 @@ __device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x
     }
 }
 
+__device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
+                                                  int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                  float *__restrict__ recv_s)
+{
+    uint4 a, b;
+    q8_item_load(x, H, t, seg, a, b);
+    fp8_item_store(H, k, seg, p0, p1, a, b, recv_q, recv_s);
+}
+
 // MXFP8 (E4M3 elements, E8M0 scale per 32 columns): the codes of the 16
 // columns [16c, 16c + 16) and their block's scale byte.  Two consecutive
 // lanes cover a block: every lane of the warp calls this.
-__device__ __forceinline__ uint4 mx_quant16(const uint16_t *__restrict__ xrow, int c, bool act, uint8_t &e_out)
+__device__ __forceinline__ uint4 mx_quant16_regs(const uint4 &a, const uint4 &b, uint8_t &e_out)
 {
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-    if (act) {
-        a = ld_stream16(xrow + (size_t)c * 16);
-        b = ld_stream16(xrow + (size_t)c * 16 + 8);
-    }
     const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float f[16];
 #pragma unroll
@@ -225,19 +271,25 @@ __device__ __forceinline__ uint4 mx_quant16(const uint16_t *__restrict__ xrow, i
     return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// MXFP8: two lanes per 32-column block, E8M0 scale byte.
-__device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,
-                                                    int seg, int p0, int p1, uint8_t *__restrict__ recv_q,
-                                                    uint8_t *__restrict__ recv_e)
+__device__ __forceinline__ uint4 mx_quant16(const uint16_t *__restrict__ xrow, int c, bool act, uint8_t &e_out)
+{
+    uint4 a, b;
+    load16(xrow, c, act, a, b);
+    return mx_quant16_regs(a, b, e_out);
+}
+
+// MXFP8: two lanes per 32-column block, E8M0 scale byte.  The store half
+// takes the item's values from q8_item_load.
+__device__ __forceinline__ void mxfp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a,
+                                                 const uint4 &b, uint8_t *__restrict__ recv_q,
+                                                 uint8_t *__restrict__ recv_e)
 {
     const int lane = threadIdx.x & 31;
     const int nb = H / 32;  // scale bytes per row
-    ItemPos it{t, seg};
-    const uint16_t *xrow = x + (size_t)it.t * H;
-    const int c = it.seg * 32 + lane;
+    const int c = seg * 32 + lane;
     const bool act = c < H / 16;  // H / 16 is even: lane pairs are wholly in or out
     uint8_t eb;
-    const uint4 qv = mx_quant16(xrow, c, act, eb);
+    const uint4 qv = mx_quant16_regs(a, b, eb);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)
@@ -246,6 +298,15 @@ __device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__
         if ((c & 1) == 0)
             recv_e[(size_t)p * nb + (c >> 1)] = eb;
     }
+}
+
+__device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,
+                                                    int seg, int p0, int p1, uint8_t *__restrict__ recv_q,
+                                                    uint8_t *__restrict__ recv_e)
+{
+    uint4 a, b;
+    q8_item_load(x, H, t, seg, a, b);
+    mxfp8_item_store(H, k, seg, p0, p1, a, b, recv_q, recv_e);
 }
 
 }  // namespace ep
