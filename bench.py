@@ -264,7 +264,8 @@ class PathRunner:
                               err_flag=self.err)
 
     def route(self):
-        """Gating and layout in one call (one cooperative launch)."""
+        """Gating and layout in one call (one cooperative launch above 4096
+        entries, as on the bench's workload)."""
         c = self.cfg
         self.ep.ep_gate_layout(self.scores, self.bias, self.gcfg, c["experts_per_rank"], topk_idx=self.topk_idx,
                                topk_w=self.topk_w, out=self.lay, workspace=self.ws, err_flag=self.err)
