@@ -178,6 +178,32 @@ __device__ __forceinline__ uint4 fp8_quant16_regs(const uint4 &a, const uint4 &b
             q[i] = ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
                    (w1 & 0x80000000u);
         }
+    } else if (s >= 0x1p-90f && s <= 0x1p125f) {
+        // x / s without a division per element, by Markstein's correction
+        // step (P. Markstein, "Computation of elementary functions on the IBM
+        // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+        // r the correctly rounded 1/s and q0 = x*r, the remainder e = s*q0 - x
+        // is exact in one FMA, and q0 - e*r rounded once is the IEEE
+        // quotient.  For bf16 x this holds for every pair of significands at
+        // every exponent gap that gives a nonzero code (an exhaustive test
+        // checks them all against IEEE division).  The scale range keeps r
+        // normal and the remainder above fp32 underflow for every quotient
+        // of 2^-11 or more; smaller quotients code to zero either way.  The
+        // remainder's sign convention (s*q0 - x, then q0 - e*r) keeps the
+        // sign of a zero x.
+        const float r = __frcp_rn(s);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float d[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float x = f[4 * i + j];
+                const float q0 = x * r;
+                const float e = fmaf(q0, s, -x);
+                d[j] = fmaf(-e, r, q0);
+            }
+            q[i] = pack_e4m3x2(d[0], d[1]) | (pack_e4m3x2(d[2], d[3]) << 16);
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
