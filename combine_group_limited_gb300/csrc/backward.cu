@@ -10,7 +10,9 @@
 // (The backward of the BF16 dispatch is the combine with unit weights; see
 // combine.cu.)
 //
-// One CTA per token at a time: each thread owns 16-byte column chunks; per
+// One CTA per token at a time (at k <= 2 on large batches, one warp per
+// token instead: combine_backward_warp_kernel): each thread owns 16-byte
+// column chunks; per
 // chunk it reads grad_out once and the k expert rows, writes the k scaled
 // rows, and keeps k partial dot products.  grad_y is rounded once to bf16:
 // the fp32 product p = w*g is corrected with its exact residual

@@ -20,8 +20,9 @@
 // The row is held in registers and never re-read per copy.
 // FP8: 8 consecutive lanes own one 128-column block (16 columns each); the
 // block's amax is a 3-step xor-shuffle max, the scale an IEEE fp32 division
-// by 448, each code an IEEE fp32 division then a round-to-nearest-even
-// saturating e4m3 conversion (cvt.rn.satfinite).
+// by 448, each code the IEEE fp32 quotient x / s (formed without a division
+// per element; see fp8_quant16_regs) then a round-to-nearest-even saturating
+// e4m3 conversion (cvt.rn.satfinite).
 #include "dispatch_impl.cuh"
 
 namespace ep {
