@@ -74,10 +74,18 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# The source files each timed kernel is compiled from.
+KERNEL_SOURCES = {
+    "combine_kernel": ("combine.cu", "ep_internal.cuh"),
+    "dispatch_bulk_kernel": ("dispatch.cu", "dispatch_impl.cuh", "ep_internal.cuh"),
+    "route_kernel": ("route.cu", "coop.cuh", "gate_impl.cuh", "ep_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_group_limited_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -85,16 +93,16 @@ def kernel_source_hash():
 
 def recorded_traffic(op):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernels as they are now (same source hash); else None."""
+    on the kernel as it is now (the same hash of its sources); else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("source_hash") != kernel_source_hash():
+    rec = d.get("kernels", {}).get(op)
+    if op not in KERNEL_SOURCES or not rec or rec.get("source_hash") != kernel_source_hash(op):
         return None
-    v = d.get("per_launch_bytes", {}).get(op)
-    return None if v is None else int(v)
+    return int(rec["bytes_per_launch"])
 
 
 class Replicas:

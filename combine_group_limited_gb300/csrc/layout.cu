@@ -387,15 +387,26 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         ssm[i] = 0;
     const int per_warp = ((N + kSmallWarps * 32 - 1) / (kSmallWarps * 32)) * 32;  // <= kSmallChunks * 32
     const int w0 = warp * per_warp;
+    // ev: the entry's expert, -1 for an empty slot, -2 outside the slice.  An
+    // index outside [0, E) other than -1 (including -2) is flagged here and
+    // becomes an empty slot, so -2 never comes from the caller's indices.
     int ev[kSmallChunks];
+    int bad = 0;
 #pragma unroll
     for (int c = 0; c < kSmallChunks; ++c) {
         const int i = w0 + 32 * c + lane;
-        ev[c] = (32 * c < per_warp && i < N) ? __ldg(idx + i) : -2;  // -2: outside the slice
+        int e = -2;
+        if (32 * c < per_warp && i < N) {
+            e = __ldg(idx + i);
+            if (e != -1 && !valid_expert(e, E)) {
+                bad = 1;
+                e = -1;
+            }
+        }
+        ev[c] = e;
     }
     __syncthreads();
     const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
-    int bad = 0;
 #pragma unroll
     for (int c = 0; c < kSmallChunks; ++c) {
         if (32 * c >= per_warp)
@@ -403,7 +414,6 @@ __global__ void __launch_bounds__(kSmallThreads) layout_small_kernel(
         const int i = w0 + 32 * c + lane;
         const int e = ev[c];
         const bool ok = valid_expert(e, E);
-        bad |= e != -2 && e != -1 && !ok;
         warp_count(s_off, ok ? (unsigned)e : 0u, ok, eb);
         if (e != -2)
             s_rank[i] = ok ? e / epr : -1;

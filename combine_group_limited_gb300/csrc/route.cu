@@ -182,18 +182,29 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
     // each warp owns a contiguous slice of at most kRtChunks x 32 entries
     const int per_warp = ((n + kRtWarps * 32 - 1) / (kRtWarps * 32)) * 32;
     const int w0 = warp * per_warp;
+    // ev: the entry's expert, -1 for an empty slot, -2 outside the slice.  An
+    // index outside [0, E) other than -1 (including -2) is flagged here and
+    // becomes an empty slot, so -2 never comes from the caller's indices.
     int ev[kRtChunks];
+    int bad = 0;
 #pragma unroll
     for (int c = 0; c < kRtChunks; ++c) {
         const int i = w0 + 32 * c + lane;
-        ev[c] = (32 * c < per_warp && i < n) ? __ldcg(a.topk_idx + n_lo + i) : -2;  // -2: outside
+        int e = -2;
+        if (32 * c < per_warp && i < n) {
+            e = __ldcg(a.topk_idx + n_lo + i);
+            if (e != -1 && (unsigned)e >= (unsigned)E) {
+                bad = 1;
+                e = -1;
+            }
+        }
+        ev[c] = e;
     }
     __syncthreads();
 
     // 2. per-warp counts (a warp's own column: no atomics) and entry ranks
     const int eb = key_bits((unsigned)E), rb = key_bits((unsigned)R);
     int32_t *my = s_wh + warp;  // my[key * kRtWhStride]
-    int bad = 0;
 #pragma unroll
     for (int c = 0; c < kRtChunks; ++c) {
         if (32 * c >= per_warp)
@@ -201,7 +212,6 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const RouteArgs a)
         const int i = w0 + 32 * c + lane;
         const int e = ev[c];
         const bool ok = (unsigned)e < (unsigned)E;
-        bad |= e != -2 && e != -1 && !ok;
         const int key = ok ? e : E;
         const unsigned grp = peer_mask((unsigned)key, eb);
         if (ok && lane == __ffs(grp) - 1)

@@ -80,6 +80,39 @@ def test_layout_out_of_range_flagged_and_skipped(ep):
     assert g["pos"].reshape(500, 4)[3, 1] == -1
 
 
+BAD_VALUES = np.array([-2, -3, -2**31, 2**31 - 1], np.int64)
+
+
+@pytest.mark.parametrize("T,k,E,epr", [(300, 8, 64, 8), (4096, 1, 16, 2), (40, 64, 1024, 16),
+                                       (3000, 6, 64, 8), (20000, 8, 256, 8)])
+def test_every_invalid_index_value_is_flagged_and_skipped(ep, T, k, E, epr):
+    """Any index outside [0, E) other than -1 -- including -2, INT_MIN and
+    INT_MAX -- is flagged and becomes an empty slot, on the one-CTA layout
+    (T*k <= 4096), the cooperative layout and the capacity layout."""
+    rng = np.random.default_rng(T * k + E)
+    idx = rng.integers(-1, E, size=(T, k)).astype(np.int64)
+    m = rng.random((T, k))
+    idx[m < 0.05] = rng.choice(np.append(BAD_VALUES, E), size=int((m < 0.05).sum()))
+    idx[0, 0] = -2
+    idx = idx.astype(np.int32)
+    clean = idx.copy()
+    clean[(clean < -1) | (clean >= E)] = -1
+    g, gflag = _gpu_layout(ep, idx, E, epr)
+    o = oracle.layout(clean, E, epr)
+    for key in KEYS:
+        np.testing.assert_array_equal(g[key].reshape(o[key].shape), o[key], err_msg=key)
+    assert gflag == ep.EP_FLAG_BAD_EXPERT
+    cap = max(1, (T * k) // E)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    c = ep.ep_get_layout_capacity(dev(idx), E, epr, cap, err_flag=flag)
+    torch.cuda.synchronize()
+    oc = oracle.layout_capacity(clean, E, epr, cap)
+    for key in KEYS + ("expert_dropped",):
+        got = getattr(c, key).cpu().numpy().reshape(-1)[: oc[key].size]
+        np.testing.assert_array_equal(got, oc[key].reshape(-1), err_msg="capacity " + key)
+    assert int(flag.item()) == ep.EP_FLAG_BAD_EXPERT
+
+
 def test_layout_empty_batch(ep):
     idx = np.zeros((0, 8), np.int32)
     lay = ep.ep_get_layout(torch.zeros((0, 8), dtype=torch.int32, device="cuda"), 256, 8)
