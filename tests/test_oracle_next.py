@@ -189,3 +189,50 @@ def test_dispatch_backward_of_copies_is_k_times():
     recv = oracle.dispatch_bf16(inp["x"], pos)
     gx = synth.bf16_bits_to_f32(oracle.dispatch_backward(recv, pos))
     np.testing.assert_array_equal(gx, 8 * synth.bf16_bits_to_f32(inp["x"]))    # 8 = 2^3: exact in bf16
+
+
+def test_capacity_rank_counts_brute_force():
+    """rank_count counts the kept entries of a rank's experts; rank_tokens
+    counts the tokens with at least one kept entry on the rank (a dropped
+    slot does not count its token), by direct enumeration on small cases."""
+    rng = np.random.default_rng(23)
+    for T, k, E, epr, cap in ((60, 4, 8, 2, 5), (40, 6, 12, 4, 3), (30, 3, 6, 3, 0), (25, 2, 4, 1, 100)):
+        idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
+        idx[rng.random((T, k)) < 0.3] = 1
+        lay = oracle.layout_capacity(idx, E, epr, cap)
+        pos = lay["pos"].reshape(T, k)
+        R = E // epr
+        kept_by_rank = [0] * R
+        tokens_by_rank = [0] * R
+        for t in range(T):
+            seen = set()
+            for j in range(k):
+                if pos[t, j] >= 0:
+                    r = int(idx[t, j]) // epr
+                    kept_by_rank[r] += 1
+                    seen.add(r)
+            for r in seen:
+                tokens_by_rank[r] += 1
+        assert lay["rank_count"].tolist() == kept_by_rank
+        assert lay["rank_tokens"].tolist() == tokens_by_rank
+        assert lay["rank_off"].tolist() == [r * epr * cap for r in range(R + 1)]
+
+
+def test_every_invalid_index_value_is_flagged_and_skipped():
+    """-1 is an empty slot; every other value outside [0, E) -- -2, INT_MIN,
+    E, INT_MAX -- raises the bad-expert flag and is skipped, in both the
+    plain and the capacity layout."""
+    E, epr = 8, 2
+    for bad in (-2, -3, -2 ** 31, E, 2 ** 31 - 1):
+        idx = np.array([[0, bad], [bad, 5], [3, -1]], np.int32)
+        clean = np.where(idx == bad, -1, idx).astype(np.int32)
+        lay, ref = oracle.layout(idx, E, epr), oracle.layout(clean, E, epr)
+        assert lay["err_flag"] & 1 and not ref["err_flag"]
+        for key in ("pos", "src", "expert_count", "rank_count", "rank_tokens"):
+            assert lay[key].tolist() == ref[key].tolist(), (bad, key)
+        cl, cr = oracle.layout_capacity(idx, E, epr, 2), oracle.layout_capacity(clean, E, epr, 2)
+        assert cl["err_flag"] & 1 and not cr["err_flag"]
+        for key in ("pos", "src", "expert_count", "expert_dropped", "rank_count", "rank_tokens"):
+            assert cl[key].tolist() == cr[key].tolist(), (bad, key)
+    empty = oracle.layout(np.array([[-1, -1]], np.int32), E, epr)
+    assert empty["err_flag"] == 0 and empty["pos"].tolist() == [[-1, -1]]
