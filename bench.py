@@ -39,6 +39,7 @@ METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of peak), 1×GB300"
 WORKLOAD = "dsv3"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20          # twice the 129 MB L2
+QUEUE_AHEAD_CYCLES = 200_000        # ~0.1 ms of GPU spin before each timed step (host launches get ahead)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -78,7 +79,7 @@ def measured_hbm_peak():
 KERNEL_SOURCES = {
     "combine_kernel": ("combine.cu", "ep_internal.cuh"),
     "dispatch_bulk_kernel": ("dispatch.cu", "dispatch_impl.cuh", "ep_internal.cuh"),
-    "route_kernel": ("route.cu", "coop.cuh", "gate_impl.cuh", "ep_internal.cuh"),
+    "route_kernel": ("route.cu", "coop.cuh", "gate_fast.cuh", "gate_impl.cuh", "ep_internal.cuh"),
 }
 
 
@@ -162,33 +163,85 @@ class Replicas:
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks / throttle reasons; only the samples
-    taken between mark_start() and mark_end() (the timed region) count."""
+    """SM clocks and throttle reasons sampled while the GPU works.
 
+    A thread polls NVML (libnvidia-ml through ctypes, read-only queries)
+    every millisecond, so that even a timed region of a few milliseconds
+    holds samples; where NVML cannot be loaded, `nvidia-smi -lms` is read
+    instead.  Only the samples taken between mark_start() and mark_end()
+    count."""
+
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    # NVML clocks-event reason bits of those four names
+    NVML_BITS = [0x8, 0x40, 0x20, 0x4]
     QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
-    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index, period_ms=20):
-        self.index, self.period_ms = index, period_ms
-        self.proc, self.samples, self.t0, self.t1 = None, [], None, None
+    def __init__(self, index, period_ms=1.0, uuid=None):
+        self.index, self.period_ms, self.uuid = index, period_ms, uuid
+        self.samples, self.t0, self.t1 = [], None, None
+        self.proc, self.thread, self.source = None, None, None
+        self._stop = False
 
-    def _reader(self):
+    # --- NVML
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(("GPU-%s" % self.uuid).encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _nvml_loop(self, lib, h, reasons):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            t = time.monotonic()
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    reasons(h, ctypes.byref(rs)) == 0):
+                self.samples.append((t, float(clk.value), float(mx.value),
+                                     [bool(rs.value & b) for b in self.NVML_BITS]))
+            time.sleep(self.period_ms / 1000.0)
+
+    # --- nvidia-smi fallback
+    def _smi_loop(self):
         for ln in self.proc.stdout:
-            self.samples.append((time.monotonic(), ln))
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                self.samples.append((time.monotonic(), float(f[0]), float(f[1]),
+                                     [v.lower() == "active" for v in f[3:7]]))
+            except ValueError:
+                continue
 
     def __enter__(self):
         import threading
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._reader, daemon=True)
+            lib, h, reasons = self._nvml_open()
+            self.thread = threading.Thread(target=self._nvml_loop, args=(lib, h, reasons), daemon=True)
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                              "--format=csv,noheader,nounits", "-lms", "20"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+                self.source = "nvidia-smi"
+            except OSError:
+                self.thread = None
+        if self.thread is not None:
             self.thread.start()
-        except OSError:
-            self.proc = None
-        time.sleep(0.5)
+        time.sleep(0.1)
         return self
 
     def mark_start(self):
@@ -198,33 +251,26 @@ class ClockSampler:
         self.t1 = time.monotonic()
 
     def __exit__(self, *a):
+        self._stop = True
         if self.proc is not None:
-            time.sleep(2 * self.period_ms / 1000)
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=5)
 
     def summary(self):
-        rows = []
-        for ts, ln in self.samples:
-            if self.t0 is None or not (self.t0 <= ts <= (self.t1 or ts)):
-                continue
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                rows.append((float(f[0]), float(f[1]), [v.lower() == "active" for v in f[3:7]]))
-            except ValueError:
-                continue
+        rows = [(c, m, r) for ts, c, m, r in list(self.samples)
+                if self.t0 is not None and self.t0 <= ts <= (self.t1 or ts)]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "no nvidia-smi sample fell inside the timed region"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source,
+                    "note": "no sample fell inside the timed region"}
         reasons = sorted({self.NAMES[i] for _, _, r in rows for i, a in enumerate(r) if a})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": self.source}
 
 
 class PathRunner:
@@ -312,9 +358,14 @@ def run_ours(args):
         # Evict the step's data from L2: write a buffer twice the L2 size,
         # then read another one so that the written lines are back in HBM
         # before the timed events (L2 is write-back; otherwise the next
-        # step would pay for writing the flush buffer).
+        # step would pay for writing the flush buffer).  Then keep the GPU
+        # busy for a while (a spin kernel, outside the events), so that the
+        # host has enqueued the step's launches before the GPU reaches the
+        # first event: the events then time the kernels, not the host's
+        # launch calls.
         flush.fill_(s & 0xFF)
         flush_rd.sum()
+        torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
 
     ops = ("route", "dispatch", "combine")
 
@@ -591,6 +642,7 @@ def run_sweep(args):
         for i in range(reps + 3):
             flush.fill_(i & 0xFF)
             flush_rd.sum()
+            torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()

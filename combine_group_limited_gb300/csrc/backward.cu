@@ -295,13 +295,8 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
     if (T == 0)
         return cudaSuccess;
     if (k <= 2 && T >= 2048) {
-        static int per_sm = 0;
-        if (per_sm < 1) {
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_backward_warp_kernel,
-                                                          kBwdWarpThreads, 0);
-            if (per_sm < 1)
-                per_sm = 1;
-        }
+        static PerDeviceCache<1> occ;
+        const int per_sm = occupancy_per_sm(occ, (const void *)combine_backward_warp_kernel, kBwdWarpThreads, 0);
         const long long need = ((long long)T + kBwdWarpThreads / 32 - 1) / (kBwdWarpThreads / 32);
         long long g = (long long)device_sm_count() * per_sm;
         if (g > need)
@@ -311,8 +306,8 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
         return cudaGetLastError();
     }
     const int threads = chunk_threads(H / 8, k);  // <= kBwdThreads (k <= 64)
-    static int cached_threads = 0, cached_per_sm = 0;
-    const int grid = row_grid((const void *)combine_backward_kernel, threads, T, cached_threads, cached_per_sm);
+    static PerDeviceCache<33> occ;
+    const int grid = row_grid((const void *)combine_backward_kernel, threads, T, occ);
     combine_backward_kernel<<<grid, threads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y, grad_w, rows,
                                                       err_flag);
     return cudaGetLastError();

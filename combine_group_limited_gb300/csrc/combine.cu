@@ -66,16 +66,12 @@ int column_segments(int T, int chunks, int resident)
 }
 
 // A persistent grid of every resident CTA of the kernel at this block size
-// (at most one per row), the occupancy cached for the last size asked.
-int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cached_per_sm)
+// (at most one per row); the occupancy is cached per device and per block
+// size (a multiple of 32, at most 1024).
+int row_grid(const void *kern, int threads, int T, PerDeviceCache<33> &cache)
 {
-    if (cached_threads != threads) {
-        int per_sm = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
-        cached_per_sm = per_sm < 1 ? 1 : per_sm;
-        cached_threads = threads;
-    }
-    const long long g = (long long)device_sm_count() * cached_per_sm;
+    const int per_sm = occupancy_per_sm(cache, kern, threads, 0, threads / 32);
+    const long long g = (long long)device_sm_count() * per_sm;
     return (int)(g < T ? g : T);
 }
 
@@ -493,12 +489,8 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
     if (T == 0)
         return cudaSuccess;
     if (k <= 2 && T >= 2048) {
-        static int wps = 0;
-        if (wps < 1) {
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&wps, (const void *)combine_warp_kernel, kCombThreads, 0);
-            if (wps < 1)
-                wps = 1;
-        }
+        static PerDeviceCache<1> occ;
+        const int wps = occupancy_per_sm(occ, (const void *)combine_warp_kernel, kCombThreads, 0);
         const long long need = ((long long)T + kCombThreads / 32 - 1) / (kCombThreads / 32);
         long long g = (long long)device_sm_count() * wps;
         if (g > need)
@@ -506,12 +498,8 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
         combine_warp_kernel<<<(int)g, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag);
         return cudaGetLastError();
     }
-    static int per_sm = 0;  // the same registers either way: sized on the unsplit kernel
-    if (per_sm < 1) {
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)combine_kernel<false>, kCombThreads, 0);
-        if (per_sm < 1)
-            per_sm = 1;
-    }
+    static PerDeviceCache<1> occ;  // the same registers either way: sized on the unsplit kernel
+    const int per_sm = occupancy_per_sm(occ, (const void *)combine_kernel<false>, kCombThreads, 0);
     const int S = column_segments(T, H / 8, device_sm_count() * per_sm);
     long long grid = (long long)device_sm_count() * per_sm;
     if (grid > (long long)T * S)
@@ -533,14 +521,9 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
     if (T == 0)
         return cudaSuccess;
     if (k <= 2 && T >= 2048) {
-        static int wps[2] = {0, 0};
+        static PerDeviceCache<2> occ;
         const void *wk = mx ? (const void *)combine_fp8_warp_kernel<true> : (const void *)combine_fp8_warp_kernel<false>;
-        int &ps = wps[mx ? 1 : 0];
-        if (ps < 1) {
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, wk, kFp8WarpThreads, 0);
-            if (ps < 1)
-                ps = 1;
-        }
+        const int ps = occupancy_per_sm(occ, wk, kFp8WarpThreads, 0, mx ? 1 : 0);
         const long long need = ((long long)T + kFp8WarpThreads / 32 - 1) / (kFp8WarpThreads / 32);
         long long g = (long long)device_sm_count() * ps;
         if (g > need)
@@ -553,15 +536,10 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
                                                                            err_flag);
         return cudaGetLastError();
     }
-    static int per_sm_cache[2] = {0, 0};
+    static PerDeviceCache<2> occ;
     const void *kern =
         mx ? (const void *)combine_fp8_kernel<true, false> : (const void *)combine_fp8_kernel<false, false>;
-    int &per_sm = per_sm_cache[mx ? 1 : 0];
-    if (per_sm < 1) {
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombThreads, 0);
-        if (per_sm < 1)
-            per_sm = 1;
-    }
+    const int per_sm = occupancy_per_sm(occ, kern, kCombThreads, 0, mx ? 1 : 0);
     const int S = column_segments(T, H / 16, device_sm_count() * per_sm);
     long long gl = (long long)device_sm_count() * per_sm;
     if (gl > (long long)T * S)

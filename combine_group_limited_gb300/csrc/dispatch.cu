@@ -273,9 +273,11 @@ size_t bulk_smem(int H, int mode)
 // to 4 %) and loses at k = 2 (Mixtral shape) and on decode-sized batches,
 // which keep the warp-item kernels -- as do rows too long to stage twice in
 // shared memory.
+constexpr size_t kBulkMaxSmem = 200 * 1024;
+
 bool use_bulk(int T, int H, int k, int mode)
 {
-    return k >= 4 && T >= 2048 && bulk_smem(H, mode) <= 200 * 1024;
+    return k >= 4 && T >= 2048 && bulk_smem(H, mode) <= kBulkMaxSmem;
 }
 
 template <int kMode>
@@ -288,13 +290,10 @@ cudaError_t launch_bulk(const uint16_t *x, int T, int H, int k, const int32_t *p
     const size_t smem = bulk_smem(H, kMode);
     const int bulk_sc = kMode != 0 && sc_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(recv_sc) & 15) == 0;
     const void *fn = (const void *)dispatch_bulk_kernel<kMode>;
-    static size_t attr_smem = 48 * 1024;  // per mode; raised to the largest staging seen
-    if (smem > attr_smem) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        attr_smem = smem;
-    }
+    static PerDeviceCache<1> attr;  // per mode: the largest staging use_bulk admits, once per device
+    const cudaError_t ae = raise_smem_limit(attr, fn, kBulkMaxSmem);
+    if (ae != cudaSuccess)
+        return ae;
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBulkThreads, smem);
     if (e != cudaSuccess)
@@ -308,22 +307,19 @@ cudaError_t launch_bulk(const uint16_t *x, int T, int H, int k, const int32_t *p
     return cudaGetLastError();
 }
 
-// A persistent grid of (resident CTAs per SM) x (SMs), capped by the work.
-int persistent_grid(const void *kernel, int &per_sm_cache, long long warp_items)
+// A persistent grid of (resident CTAs per SM) x (SMs), capped by the work;
+// the occupancy is cached per device.
+int persistent_grid(const void *kernel, PerDeviceCache<1> &per_sm_cache, long long warp_items)
 {
-    if (per_sm_cache < 1) {
-        int per_sm = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDispThreads, 0);
-        per_sm_cache = per_sm < 1 ? 1 : per_sm;
-    }
-    const long long g = (long long)device_sm_count() * per_sm_cache;
+    const int per_sm = occupancy_per_sm(per_sm_cache, kernel, kDispThreads, 0);
+    const long long g = (long long)device_sm_count() * per_sm;
     const long long need = (warp_items + kDispThreads / 32 - 1) / (kDispThreads / 32);
     return (int)(need < g ? need : g);
 }
 
-int g_bf16_per_sm = 0;
-int g_fp8_per_sm = 0;
-int g_mx_per_sm = 0;
+PerDeviceCache<1> g_bf16_per_sm;
+PerDeviceCache<1> g_fp8_per_sm;
+PerDeviceCache<1> g_mx_per_sm;
 
 }  // namespace
 

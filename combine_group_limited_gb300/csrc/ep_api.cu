@@ -7,21 +7,25 @@
 
 namespace ep {
 
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    return dev;
+}
+
 int device_sm_count()
 {
     // Cached per device; the attribute never changes for a device.
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
-        return 1;
-    if (dev < 64 && cache[dev] > 0)
-        return cache[dev];
-    int n = 1;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-        n = 1;
-    if (dev < 64)
-        cache[dev] = n;
-    return n;
+    static PerDeviceCache<1> cache;
+    return cache.get([] {
+        const int dev = current_device();
+        int n = 1;
+        if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        return n;
+    });
 }
 
 }  // namespace ep
@@ -184,12 +188,20 @@ ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, cons
         return EP_ERR_ALIGNMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ep::GateParams gp = gate_params(cfg);
-    if ((long long)T * k > ep::kSmallLayoutEntries && ep::route_supported(T, k, E))
+    // The grid-wide launch with lane-segment gating for group-limited
+    // batches past decode size and for batches past one cluster's layout;
+    // otherwise the gate kernel then the layout (one CTA, or one cluster).
+    const long long entries = (long long)T * k;
+    const bool grouped = gp.Kg < gp.G;
+    if (T > 0 && entries > ep::kSmallLayoutEntries && (grouped || entries > ep::kClusterLayoutEntries) &&
+        ep::route_supported(T, k, E, experts_per_rank, true) && ep::gate_fast_supported(gp, scores, bias))
         return launched(ep::launch_route(scores, bias, &gp, nullptr, topk_idx, topk_w, T, k, E, experts_per_rank,
                                          expert_count, expert_off, rank_count, rank_off, rank_tokens, pos, src,
                                          err_flag, workspace, st));
-    // one-CTA layouts and batches too large for the single launch: the two
-    // steps' own kernels
+    // batches of at most 4096 entries (the gate kernel and the one-CTA
+    // layout: a grid-wide launch only adds latency there), configurations
+    // the lane-segment gating does not serve, and batches too large for one
+    // grid of one CTA per SM: the two steps' own kernels
     cudaError_t e = ep::launch_gate(scores, bias, T, gp, topk_idx, topk_w, st);
     if (e == cudaSuccess)
         e = ep::launch_layout(topk_idx, T, k, E, experts_per_rank, expert_count, expert_off, rank_count, rank_off,

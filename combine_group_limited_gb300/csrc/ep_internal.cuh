@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ep {
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
@@ -111,6 +113,22 @@ struct GateParams {
 cudaError_t launch_gate(const float *scores, const float *bias, int T, const GateParams &p,
                         int32_t *topk_idx, float *topk_w, cudaStream_t st);
 
+// Whether launch_gate takes the lane-segment kernel (gate_fast.cuh) for
+// this configuration and these pointers; the warp-per-token kernel serves
+// the rest.
+bool gate_fast_supported(const GateParams &p, const float *scores, const float *bias);
+
+// The dispatch layout (capacity mode when cap >= 0) by one thread-block
+// cluster in one launch, with no workspace (layout_cluster.cu).  Launched
+// with programmatic stream serialisation.  supported() says whether this
+// device and these sizes fit it; the launch returns cudaErrorNotSupported
+// otherwise.
+bool layout_cluster_supported(int T, int k, int E, int epr);
+cudaError_t launch_layout_cluster(const int32_t *topk_idx, int T, int k, int E, int epr, int cap,
+                                  int32_t *expert_count, int32_t *expert_off, int32_t *rank_count,
+                                  int32_t *rank_off, int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos,
+                                  int32_t *src, int32_t *err_flag, cudaStream_t st);
+
 int layout_tile_tokens(int k);
 int layout_num_tiles(int T, int k);
 size_t layout_workspace_bytes(int T, int k, int E, int epr);
@@ -152,16 +170,23 @@ cudaError_t launch_decode(const float *scores, const float *bias, int T, const G
 cudaError_t launch_barrier_selftest(unsigned extra, long long spin_limit, int32_t *err_flag, void *barrier_word,
                                     cudaStream_t st);
 
-// Gating (gp != NULL, scores -> topk_idx, topk_w) and/or layout (of
-// topk_idx_in when gp == NULL; capacity mode when cap >= 0, src then cleared
-// to -1 beforehand) in one cooperative launch.  workspace: at
-// least route_workspace_bytes(E), 16-byte aligned; its first word (the grid
-// barrier's arrival count) zero, and left zero by every call that completes.
+// Gating (gp != NULL: scores -> topk_idx, topk_w, with the lane-segment
+// body) and the layout of the chosen experts, or the layout of topk_idx_in
+// (gp == NULL; capacity mode when cap >= 0) -- one cooperative launch
+// (route.cu).  workspace: at least route_workspace_bytes(E), 16-byte
+// aligned; its first word (the grid barrier's arrival count) zero, and left
+// zero by every call that completes.  route_supported says whether the
+// sizes fit one grid of one CTA per SM (and, when gating, whether the
+// lane-segment body serves the configuration).
 size_t route_workspace_bytes(int E);
-bool route_supported(int T, int k, int E);
+bool route_supported(int T, int k, int E, int epr, bool gate);
+// The grid and cluster size the cooperative routing launch takes for T tokens.
+void route_launch_shape(int T, int *grid, int *cluster);
 
 // Layouts of at most this many entries (T*k) run as one kernel on one CTA.
 constexpr int kSmallLayoutEntries = 4096;
+// Layouts of at most this many entries take the one-cluster kernel.
+constexpr long long kClusterLayoutEntries = 65536;
 cudaError_t launch_route(const float *scores, const float *bias, const GateParams *gp, const int32_t *topk_idx_in,
                          int32_t *topk_idx, float *topk_w, int T, int k, int E, int epr, int32_t *expert_count,
                          int32_t *expert_off, int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens,
@@ -170,8 +195,72 @@ cudaError_t launch_route(const float *scores, const float *bias, const GateParam
 
 int device_sm_count();
 
-// Launch shape of the CTA-per-row kernels (defined in combine.cu).
+// The current device, or -1 if it cannot be read.
+int current_device();
+
+constexpr int kMaxDevices = 64;
+
+// Host-side values worth computing once per device: a kernel attribute that
+// has been raised (cudaFuncSetAttribute acts per device), an occupancy
+// figure, the SM count.  Slot [device][key] holds a positive value once
+// computed.  The slots are atomics, so host threads may call concurrently; a
+// first use on two threads at once computes the value twice, which is
+// harmless because both get the same value.  A device past kMaxDevices is
+// served by computing every time.
+template <int kKeys = 1>
+struct PerDeviceCache {
+    std::atomic<int> v[kMaxDevices][kKeys];
+
+    // The cached value for (current device, key), else f(): cached when > 0,
+    // returned uncached otherwise (a failure is retried on the next call).
+    template <class F>
+    int get(F &&f, int key = 0)
+    {
+        const int d = current_device();
+        if (d < 0 || d >= kMaxDevices || key < 0 || key >= kKeys)
+            return f();
+        int x = v[d][key].load(std::memory_order_acquire);
+        if (x > 0)
+            return x;
+        x = f();
+        if (x > 0)
+            v[d][key].store(x, std::memory_order_release);
+        return x;
+    }
+};
+
+// Resident CTAs per SM of `kernel` at this block size and dynamic shared
+// memory (at least 1), cached per device in slot `key` of `cache`.
+template <int kKeys>
+inline int occupancy_per_sm(PerDeviceCache<kKeys> &cache, const void *kernel, int threads, size_t smem, int key = 0)
+{
+    return cache.get(
+        [&] {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            return per_sm;
+        },
+        key);
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device.  Returns the CUDA error of the first failing try.
+inline cudaError_t raise_smem_limit(PerDeviceCache<1> &cache, const void *kernel, size_t bytes)
+{
+    cudaError_t err = cudaSuccess;
+    cache.get([&] {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        return err == cudaSuccess ? 1 : 0;
+    });
+    return err;
+}
+
+// Launch shape of the CTA-per-row kernels (defined in combine.cu): a grid
+// of every resident CTA (occupancy cached per device and block size in
+// `cache`), at most one per row.
 int chunk_threads(int c, int k);
-int row_grid(const void *kern, int threads, int T, int &cached_threads, int &cached_per_sm);
+int row_grid(const void *kern, int threads, int T, PerDeviceCache<33> &cache);
 
 }  // namespace ep

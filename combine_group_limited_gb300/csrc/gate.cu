@@ -20,7 +20,7 @@
 // its next key.  Only at the end does a lane find which of its experts its
 // won keys were (equal keys lowest index first).  The unbiased score of each
 // chosen expert is re-read from the (cached) score row.
-#include "gate_impl.cuh"
+#include "gate_fast.cuh"
 
 namespace ep {
 
@@ -57,13 +57,83 @@ cudaError_t launch_epl(const float *scores, const float *bias, int T, const Gate
     return cudaGetLastError();
 }
 
+template <int EPL, int L, int Q>
+cudaError_t launch_fast_q(const GateFastPlan &f, const float *scores, const float *bias, int T, const GateParams &p,
+                          int32_t *idx, float *w, cudaStream_t st)
+{
+    GateFastArgs a{};
+    a.scores = scores;
+    a.bias = bias;
+    a.T = T;
+    a.p = p;
+    a.m = f.m;
+    a.q = f.q;
+    a.topk_idx = idx;
+    a.topk_w = w;
+    a.cap = f.cap;
+    const size_t smem = gate_fast_smem<EPL, L>(a.cap, p.k);
+    const void *fn = (const void *)gate_fast_kernel<EPL, L, Q>;
+    static PerDeviceCache<1> attr;  // the largest size any call can need (k = 32), once per device
+    const cudaError_t e = raise_smem_limit(attr, fn, gate_fast_smem<EPL, L>(kGfCap, 32));
+    if (e != cudaSuccess)
+        return e;
+    constexpr int TPC = kGfThreads / L;
+    gate_fast_kernel<EPL, L, Q><<<(T + TPC - 1) / TPC, kGfThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int EPL, int L>
+cudaError_t launch_fast_l(const GateFastPlan &f, const float *scores, const float *bias, int T, const GateParams &p,
+                          int32_t *idx, float *w, cudaStream_t st)
+{
+    if (f.Q == 1)
+        return launch_fast_q<EPL, L, 1>(f, scores, bias, T, p, idx, w, st);
+    if (f.Q == 2)
+        return launch_fast_q<EPL, L, 2>(f, scores, bias, T, p, idx, w, st);
+    return launch_fast_q<EPL, L, 4>(f, scores, bias, T, p, idx, w, st);
+}
+
+cudaError_t launch_fast(const GateFastPlan &f, const float *scores, const float *bias, int T, const GateParams &p,
+                        int32_t *idx, float *w, cudaStream_t st)
+{
+    switch (p.E) {
+    case 8: return launch_fast_l<8, 1>(f, scores, bias, T, p, idx, w, st);
+    case 16: return launch_fast_l<8, 2>(f, scores, bias, T, p, idx, w, st);
+    case 32: return launch_fast_l<8, 4>(f, scores, bias, T, p, idx, w, st);
+    case 64: return launch_fast_l<8, 8>(f, scores, bias, T, p, idx, w, st);
+    case 128: return launch_fast_l<16, 8>(f, scores, bias, T, p, idx, w, st);
+    default: return launch_fast_l<32, 8>(f, scores, bias, T, p, idx, w, st);
+    }
+}
+
 }  // namespace
+
+bool gate_fast_supported(const GateParams &p, const float *scores, const float *bias)
+{
+    GateFastPlan f;
+    return gate_fast_plan(p, scores, bias, f);
+}
+
+// The lane-segment kernel serves group-limited gating of batches of 2048 or
+// more tokens: measured on GB300 it is faster there (DeepSeek-V3 shape:
+// 12.1 against 13.1 us cold, 8.3 against 10.4 us back to back).  Elsewhere
+// the warp-per-token kernel measured as fast or faster: its shorter chains
+// win on decode-sized batches (3.2 against 6.4 us back to back), and
+// without groups it loses nothing to the lane segments' per-lane work.
+bool use_gate_fast(const GateParams &p, int T, const float *scores, const float *bias)
+{
+    GateFastPlan f;
+    return T >= 2048 && p.Kg < p.G && gate_fast_plan(p, scores, bias, f);
+}
 
 cudaError_t launch_gate(const float *scores, const float *bias, int T, const GateParams &p,
                         int32_t *topk_idx, float *topk_w, cudaStream_t st)
 {
     if (T == 0)
         return cudaSuccess;
+    GateFastPlan f;
+    if (use_gate_fast(p, T, scores, bias) && gate_fast_plan(p, scores, bias, f))
+        return launch_fast(f, scores, bias, T, p, topk_idx, topk_w, st);
     if (p.E <= 32)
         return launch_epl<1>(scores, bias, T, p, topk_idx, topk_w, st);
     if (p.E <= 64)

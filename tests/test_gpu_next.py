@@ -175,7 +175,7 @@ def test_capacity_layout_extremes_with_skips(ep, cap):
 def test_capacity_layout_bad_indices_and_large_batches(ep, T, k, E, epr, cap):
     """Out-of-range indices are flagged and skipped in capacity mode too;
     100000 tokens run the three-launch kernels (a grid of one CTA per SM would
-    hold more than 4096 entries per CTA), 3000 the single launch."""
+    hold more than 128 tokens per CTA), 3000 the one-cluster kernel."""
     rng = np.random.default_rng(T + cap)
     idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
     idx[rng.random((T, k)) < 0.002] = E + 3

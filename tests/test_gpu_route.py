@@ -1,9 +1,10 @@
-"""GPU parity of the routing call ep_gate_layout (gating and layout in one
-cooperative launch above 4096 entries, the gate kernel and the one-CTA
-layout below) and of ep_get_layout's cooperative path for batches of more
-than 4096 entries, against the CPU oracle and against the separate calls;
-the grid barrier's bounded wait reports a workspace whose barrier words are
-not clear."""
+"""GPU parity of the routing call ep_gate_layout (one grid-wide launch for
+group-limited batches past 4096 entries and for batches past 65536 entries;
+the gate kernel then the one-CTA or one-cluster layout otherwise) and of
+ep_get_layout past 4096 entries (one cluster, the grid-wide launch, or three
+launches for the largest batches), against the CPU oracle and against the
+separate calls; the grid barrier's bounded wait reports a workspace whose
+barrier words are not clear."""
 import numpy as np
 import pytest
 import torch
@@ -78,8 +79,9 @@ def test_gate_layout_repeated_on_one_workspace(ep):
 @pytest.mark.parametrize("T,k,E,epr", [(2000, 4, 64, 8), (4097, 1, 16, 2), (30000, 8, 256, 8), (600, 64, 1024, 16),
                                        (70000, 8, 160, 20)])
 def test_cooperative_layout_random_with_skips_and_bad_indices(ep, T, k, E, epr):
-    """More than 4096 entries: ep_get_layout's single launch, on index
-    tensors with -1 slots, repeated experts and out-of-range values."""
+    """More than 4096 entries (the one-cluster, grid-wide and three-launch
+    layouts), on index tensors with -1 slots, repeated experts and
+    out-of-range values."""
     rng = np.random.default_rng(T + k + E)
     idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
     idx[rng.random((T, k)) < 0.001] = E + 5
