@@ -328,6 +328,11 @@ class PathRunner:
         self.ep.ep_dispatch(self.x, self.lay.pos, "fp8", recv=self.recv_q, recv_scales=self.recv_s,
                             err_flag=self.err)
 
+    def dispatch_bf16(self):
+        if not hasattr(self, "recv_b"):
+            self.recv_b = self.torch.empty_like(self.y)
+        self.ep.ep_dispatch(self.x, self.lay.pos, "bf16", recv=self.recv_b, err_flag=self.err)
+
     def combine(self):
         self.ep.ep_combine(self.y, self.lay.pos, self.topk_w, out=self.out, err_flag=self.err)
 
@@ -335,6 +340,73 @@ class PathRunner:
         self.route()
         self.dispatch()
         self.combine()
+
+
+def pct(xs, q):
+    """The q-th percentile (0..100) of xs, by linear interpolation."""
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+# Every workload of the benchmark's configuration list, with the dispatch
+# payloads it is quoted with (the first one is the step's); each gets its
+# routing, dispatch and combine timed in the bench line's "configs".
+CONFIG_RUNS = {
+    "tiny": ("bf16",),
+    "mixtral": ("bf16",),
+    "dsv3": ("fp8", "bf16"),
+    "skewed": ("fp8", "bf16"),
+    "qwen3": ("bf16",),
+    "decode": ("fp8", "bf16"),
+}
+
+
+def time_configs(reps, peak, flush_l2):
+    """Per workload: mean, median, p10 and p90 event times of each op over
+    `reps` L2-flushed calls, GB/s and fraction of the HBM peak from its
+    algorithmic bytes and the mean time, and the tokens/s of one routing +
+    dispatch + combine step (means)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, payloads in CONFIG_RUNS.items():
+        cfg = synth.config(name)
+        r = PathRunner(cfg)
+        nb = op_bytes(cfg)
+        ops = [("route", r.route, nb["gate_layout"])]
+        for p in payloads:
+            fn = r.dispatch if p == "fp8" else r.dispatch_bf16
+            ops.append(("dispatch_" + p, fn, nb["dispatch_" + p]))
+        ops.append(("combine", r.combine, nb["combine"]))
+        res = {}
+        for op, fn, nbytes in ops:
+            fn()
+            ts = []
+            for i in range(reps + 2):
+                flush_l2(i)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            # The event clock ticks in steps of about 2 us on this GPU: the
+            # mean over the repetitions (random phase) resolves below a tick
+            # and gives the rates; the percentiles show the spread.
+            mean = statistics.mean(ts)
+            gbs = nbytes / (mean * 1e-6) / 1e9
+            res[op] = {"us": round(mean, 2), "us_median": round(pct(ts, 50), 2), "us_p10": round(pct(ts, 10), 2),
+                       "us_p90": round(pct(ts, 90), 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                       "bytes": nbytes}
+        if int(r.err.item()) != 0:
+            raise RuntimeError("device error flag set on %s: %d" % (name, int(r.err.item())))
+        step_us = res["route"]["us"] + res["dispatch_" + payloads[0]]["us"] + res["combine"]["us"]
+        out[name] = {"T": cfg["T"], "H": cfg["H"], "E": cfg["E"], "k": cfg["k"],
+                     "step_dispatch": payloads[0], "step_us": round(step_us, 2),
+                     "step_tokens_per_s": round(cfg["T"] / (step_us * 1e-6), 1), "ops": res}
+        del r
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -399,6 +471,10 @@ def run_ours(args):
     e2e = run_e2e(r, args, chunks=args.e2e_chunks, graph=not args.e2e_no_graph)
     e2e["ms"] = rep.max(e2e["ms"])
 
+    configs = None
+    if rep.is_printer() and not args.no_configs:
+        configs = time_configs(args.config_reps, measured_hbm_peak()[0], flush_l2)
+
     if rep.is_printer():
         T = cfg["T"]
         peak, peak_kind = measured_hbm_peak()
@@ -409,8 +485,10 @@ def run_ours(args):
         for op in ops:
             us = 1e3 * statistics.mean(per_op[op])
             gbs = bytes_of[op] / (us * 1e-6) / 1e9
-            op_summary[op] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                              "bytes": bytes_of[op], "kernel": kname[op]}
+            op_summary[op] = {"us": round(us, 2), "us_median": round(1e3 * pct(per_op[op], 50), 2),
+                              "us_p10": round(1e3 * pct(per_op[op], 10), 2),
+                              "us_p90": round(1e3 * pct(per_op[op], 90), 2), "GB/s": round(gbs, 1),
+                              "frac": round(gbs / peak, 4), "bytes": bytes_of[op], "kernel": kname[op]}
         dom = max(("dispatch", "combine"), key=lambda o: op_summary[o]["us"])
         traffic = recorded_traffic(kname[dom])
         cpu = cpu_baseline(cfg, args)
@@ -422,6 +500,9 @@ def run_ours(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4),
+            "ms_per_step_median": round(pct(step_ms, 50), 4),
+            "ms_per_step_p10": round(pct(step_ms, 10), 4),
+            "ms_per_step_p90": round(pct(step_ms, 90), 4),
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -447,6 +528,7 @@ def run_ours(args):
                               % (e2e["chunks"], ", the step's calls captured once as a CUDA graph and replayed"
                                  if e2e["graph"] else "")},
             "cpu_baseline": cpu,
+            "configs": configs,
             "clocks": clk.summary(),
             "gpu_launches": PathRunner.LAUNCHES_PER_STEP * args.steps,
         }
@@ -761,6 +843,9 @@ def main():
     ap.add_argument("--e2e-no-graph", action="store_true",
                     help="issue the end-to-end leg's calls from Python every step instead of replaying a CUDA graph")
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per op in --sweep")
+    ap.add_argument("--config-reps", type=int, default=20,
+                    help="L2-flushed repetitions per op of every workload in the line's 'configs'")
+    ap.add_argument("--no-configs", action="store_true", help="leave the per-workload 'configs' out of the line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -12,10 +12,12 @@ Tolerances (u = 2^-24, the binary32 unit roundoff):
    relative error is below u*(2D + 8 + n) with D the spread of the logits
    involved; the test allows u*(2D + 10 + n).
  * combine: the stated bar is max(1 bf16 ulp, 1e-2 relative) against the
-   exact (binary64) oracle.  The kernel is specified to accumulate in fp32,
-   whose fma chain can differ from the exact sum by k*u*sum_j|w_j y_j| before
-   the final rounding; that only matters where the sum cancels, so the test
-   adds exactly that term.
+   exact (binary64) oracle, and the five workloads' full-size tests are held
+   to it alone.  The kernel is specified to accumulate in fp32, whose fma
+   chain can differ from the exact sum by k*u*sum_j|w_j y_j| before the final
+   rounding; that only matters where the sum cancels, which the synthetic
+   edge cases (signed weights, arbitrary expert outputs) provoke on purpose,
+   so those tests add exactly that term (accumulation=True).
 """
 import numpy as np
 import torch
@@ -74,8 +76,9 @@ def bf16_ulp(v):
     return np.exp2(e - 7)
 
 
-def assert_combine_close(out_gpu_bits, out_ref_bits, y_bits, pos, w):
-    """out_gpu vs out_ref (bf16 bit patterns, [T,H]) with the tolerance above."""
+def assert_combine_close(out_gpu_bits, out_ref_bits, y_bits, pos, w, accumulation=True):
+    """out_gpu vs out_ref (bf16 bit patterns, [T,H]) with the tolerance above:
+    the stated bar, plus the fp32 accumulation term when accumulation=True."""
     g = synth.bf16_bits_to_f32(out_gpu_bits).astype(np.float64)
     r = synth.bf16_bits_to_f32(out_ref_bits).astype(np.float64)
     T, k = pos.shape
@@ -85,7 +88,7 @@ def assert_combine_close(out_gpu_bits, out_ref_bits, y_bits, pos, w):
         p = pos[:, j]
         ok = p >= 0
         S[ok] += np.abs(w[ok, j].astype(np.float64))[:, None] * np.abs(yf[p[ok]].astype(np.float64))
-    tol = np.maximum(bf16_ulp(r), 1e-2 * np.abs(r)) + k * U * S
+    tol = np.maximum(bf16_ulp(r), 1e-2 * np.abs(r)) + (k * U * S if accumulation else 0.0)
     err = np.abs(g - r)
     bad = err > tol
     assert not bad.any(), "combine differs at %s: gpu %r ref %r tol %r" % (

@@ -1,6 +1,8 @@
 """GPU parity of steps 4-5 (inverse gather + weighted combine) against the
-CPU oracle, within the stated tolerance (tests/gpu_util.py), with identity
-experts (y = the dispatched rows) and with arbitrary expert outputs."""
+CPU oracle: the five workloads with identity experts (y = the dispatched
+rows) within the stated bar, max(1 bf16 ulp, 1e-2 relative); arbitrary
+expert outputs and signed weights within that bar plus the fp32
+accumulation term (tests/gpu_util.py)."""
 import numpy as np
 import pytest
 import torch
@@ -47,7 +49,7 @@ def test_combine_full_size_identity_experts(ep, name):
     pos, wh, y = lay.pos.cpu().numpy(), w.cpu().numpy(), host_bits(recv)
     r = oracle.combine(y, pos, wh)
     g = host_bits(out)
-    assert_combine_close(g, r, y, pos, wh)
+    assert_combine_close(g, r, y, pos, wh, accumulation=False)   # the stated bar alone
     # weights sum to one: the round trip gives x back to within a bf16 ulp
     x = synth.bf16_bits_to_f32(inp["x"]).astype(np.float64)
     o = synth.bf16_bits_to_f32(g).astype(np.float64)

@@ -69,9 +69,12 @@ def test_mxfp8_special_blocks(ep):
 # ------------------------------------------------------- FP8-input combine
 
 
-def _assert_fp8_combine_close(g_bits, r_bits, deq, pos, w):
-    """Stated bar max(1 bf16 ulp, 1e-2 rel) + the fp32 terms: one rounding per
-    dequantised product and one per fma, 2k*u*sum|w*d| in all."""
+def _assert_fp8_combine_close(g_bits, r_bits, deq, pos, w, accumulation=True):
+    """Stated bar max(1 bf16 ulp, 1e-2 rel), plus (accumulation=True) the
+    fp32 terms: one rounding per dequantised product and one per fma,
+    2k*u*sum|w*d| in all -- for the signed-weight edge cases, where sums
+    cancel on purpose; the workloads' identity-expert runs take the stated
+    bar alone."""
     g = synth.bf16_bits_to_f32(g_bits).astype(np.float64)
     r = synth.bf16_bits_to_f32(r_bits).astype(np.float64)
     T, k = pos.shape
@@ -79,7 +82,7 @@ def _assert_fp8_combine_close(g_bits, r_bits, deq, pos, w):
     for j in range(k):
         ok = pos[:, j] >= 0
         S[ok] += np.abs(w[ok, j].astype(np.float64))[:, None] * np.abs(deq[pos[ok, j]])
-    tol = np.maximum(bf16_ulp(r), 1e-2 * np.abs(r)) + 2 * k * U * S
+    tol = np.maximum(bf16_ulp(r), 1e-2 * np.abs(r)) + (2 * k * U * S if accumulation else 0.0)
     bad = np.abs(g - r) > tol
     assert not bad.any(), np.argwhere(bad)[:5]
 
@@ -102,7 +105,8 @@ def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     torch.cuda.synchronize()
     pos, wh, qh, sh = lay.pos.cpu().numpy(), w.cpu().numpy(), q.cpu().numpy(), s.cpu().numpy()
     r = oracle.combine_fp8(qh, sh, pos, wh)
-    _assert_fp8_combine_close(host_bits(out), r, _dequant(qh, sh, 128 if fmt == "fp8" else 32), pos, wh)
+    _assert_fp8_combine_close(host_bits(out), r, _dequant(qh, sh, 128 if fmt == "fp8" else 32), pos, wh,
+                              accumulation=False)
 
 
 @pytest.mark.parametrize("fmt,T,H,k,scale_offset", [
