@@ -24,7 +24,7 @@
 // instead of 2 bytes of BF16 halves the bytes the combine reads.
 #include <cuda_fp16.h>
 
-#include "ep_internal.cuh"
+#include "coop.cuh"
 
 namespace ep {
 
@@ -179,6 +179,34 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b)
     return b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
 }
 
+// acc (16 columns as 8 packed fp32x2 pairs) += ws * decode(16 codes): the
+// fp32 fma chain of every column, two columns per packed instruction.
+__device__ __forceinline__ void fma_codes16(uint64_t ws2, const uint4 &v, uint64_t (&acc)[8])
+{
+    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float d0, d1, d2, d3;
+        e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
+        acc[2 * i] = f2_fma(ws2, f2_pack(d0, d1), acc[2 * i]);
+        acc[2 * i + 1] = f2_fma(ws2, f2_pack(d2, d3), acc[2 * i + 1]);
+    }
+}
+
+// The 16 accumulated columns rounded to bf16 as two 16-byte words.
+__device__ __forceinline__ void pack_acc16(const uint64_t (&acc)[8], uint4 &o0, uint4 &o1)
+{
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float lo, hi;
+        f2_unpack(acc[i], lo, hi);
+        w[i] = pack_bf16x2(lo, hi);
+    }
+    o0 = make_uint4(w[0], w[1], w[2], w[3]);
+    o1 = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 // kMx: scales are E8M0 bytes per 32 columns; else fp32 per 128 columns.
 template <bool kMx, bool kSplit>
 __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t *__restrict__ yq,
@@ -225,10 +253,10 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
             nw = __ldg(w + tn * k + threadIdx.x);
         }
         for (int c = c_lo + threadIdx.x; c < c_hi; c += kCombThreads) {
-            float acc[16];
+            uint64_t acc[8];  // column pairs, packed fp32x2
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                acc[i] = 0.0f;
+            for (int i = 0; i < 8; ++i)
+                acc[i] = 0ull;
             const int sb = kMx ? (c >> 1) : (c >> 3);  // this lane's scale block
             for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
                 // First issue every load of the batch (codes and raw scale
@@ -254,33 +282,161 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
                         // rounding per term, as scaling each code would be
                         const float sc = kMx ? e8m0_to_f32(sraw[u]) : __uint_as_float(sraw[u]);
                         const float ws = s_w[j] * sc;
-                        const uint32_t vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float d0, d1, d2, d3;
-                            e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
-                            acc[4 * i] = fmaf(ws, d0, acc[4 * i]);
-                            acc[4 * i + 1] = fmaf(ws, d1, acc[4 * i + 1]);
-                            acc[4 * i + 2] = fmaf(ws, d2, acc[4 * i + 2]);
-                            acc[4 * i + 3] = fmaf(ws, d3, acc[4 * i + 3]);
-                        }
+                        fma_codes16(f2_pack(ws, ws), v[u], acc);
                     }
                 }
             }
             uint4 o0, o1;
-            o0.x = pack_bf16x2(acc[0], acc[1]);
-            o0.y = pack_bf16x2(acc[2], acc[3]);
-            o0.z = pack_bf16x2(acc[4], acc[5]);
-            o0.w = pack_bf16x2(acc[6], acc[7]);
-            o1.x = pack_bf16x2(acc[8], acc[9]);
-            o1.y = pack_bf16x2(acc[10], acc[11]);
-            o1.z = pack_bf16x2(acc[12], acc[13]);
-            o1.w = pack_bf16x2(acc[14], acc[15]);
+            pack_acc16(acc, o0, o1);
             uint16_t *dst = out + (size_t)t * H + (size_t)c * 16;
             st_stream16(dst, o0);
             st_stream16(dst + 8, o1);
         }
     }
+}
+
+// Decode-sized batches (fewer tokens than resident CTAs): one thread per
+// column chunk of one token (8 BF16 columns, or 16 FP8 codes), with no
+// shared memory and no block barrier.  Each thread reads its token's rows
+// and weights itself (the lanes of a warp read the same words, one request)
+// and then its chunk of up to 8 slots at once, so a call is two dependent
+// memory round trips.  The CTA kernels stage rows and weights in shared
+// memory behind two block barriers and, at this size, leave most of each
+// CTA idle.  Launched with programmatic stream serialisation: the launch
+// may overlap the previous kernel's tail; griddepcontrol.wait precedes
+// every global access.  The same fp32 fma chain in slot order, so the
+// results equal the CTA kernels' bit for bit.
+constexpr int kFlatThreads = 256;
+
+// Rows and weights of slots [j0, j0 + 8) of token t; a row outside [0, rows)
+// is flagged (by the token's first chunk) and skipped.
+__device__ __forceinline__ void flat_slots(const int32_t *__restrict__ pos, const float *__restrict__ w, long long t,
+                                           int k, int j0, long long rows, int32_t *err_flag, bool first,
+                                           int (&p)[kSlotBatch], float (&ww)[kSlotBatch])
+{
+#pragma unroll
+    for (int u = 0; u < kSlotBatch; ++u) {
+        const int j = j0 + u;
+        p[u] = j < k ? __ldg(pos + t * k + j) : -1;
+        ww[u] = j < k ? (w ? __ldg(w + t * k + j) : 1.0f) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSlotBatch; ++u)
+        if (p[u] >= rows) {
+            if (first && err_flag)
+                atomicOr(err_flag, 2);
+            p[u] = -1;
+        }
+}
+
+__global__ void __launch_bounds__(kFlatThreads) combine_flat_kernel(const uint16_t *__restrict__ y,
+                                                                    const int32_t *__restrict__ pos,
+                                                                    const float *__restrict__ w, int T, int H, int k,
+                                                                    uint16_t *__restrict__ out, long long rows,
+                                                                    int32_t *__restrict__ err_flag)
+{
+    pdl_wait();
+    const int C = H / 8;
+    const long long g = (long long)blockIdx.x * kFlatThreads + threadIdx.x;
+    if (g >= (long long)T * C)
+        return;
+    const long long t = g / C;
+    const int c = (int)(g - t * C);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+        int p[kSlotBatch];
+        float ww[kSlotBatch];
+        flat_slots(pos, w, t, k, j0, rows, err_flag, c == 0, p, ww);
+        uint4 v[kSlotBatch];
+#pragma unroll
+        for (int u = 0; u < kSlotBatch; ++u)
+            if (p[u] >= 0)
+                v[u] = ld_stream16(y + (size_t)p[u] * H + (size_t)c * 8);
+#pragma unroll
+        for (int u = 0; u < kSlotBatch; ++u)
+            if (p[u] >= 0) {
+                const uint32_t vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(ww[u], bf16_lo(vv[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(ww[u], bf16_hi(vv[i]), acc[2 * i + 1]);
+                }
+            }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    st_stream16(out + (size_t)t * H + (size_t)c * 8, o);
+}
+
+template <bool kMx>
+__global__ void __launch_bounds__(kFlatThreads) combine_fp8_flat_kernel(const uint8_t *__restrict__ yq,
+                                                                        const void *__restrict__ yscale,
+                                                                        const int32_t *__restrict__ pos,
+                                                                        const float *__restrict__ w, int T, int H,
+                                                                        int k, uint16_t *__restrict__ out,
+                                                                        long long rows, int32_t *__restrict__ err_flag)
+{
+    pdl_wait();
+    const int C16 = H / 16;
+    const int nb = kMx ? H / 32 : H / 128;
+    const long long g = (long long)blockIdx.x * kFlatThreads + threadIdx.x;
+    if (g >= (long long)T * C16)
+        return;
+    const long long t = g / C16;
+    const int c = (int)(g - t * C16);
+    const int sb = kMx ? (c >> 1) : (c >> 3);
+    uint64_t acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0ull;
+    for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+        int p[kSlotBatch];
+        float ww[kSlotBatch];
+        flat_slots(pos, w, t, k, j0, rows, err_flag, c == 0, p, ww);
+        uint4 v[kSlotBatch];
+        uint32_t sraw[kSlotBatch];
+#pragma unroll
+        for (int u = 0; u < kSlotBatch; ++u)
+            if (p[u] >= 0) {
+                v[u] = ld_stream16(yq + (size_t)p[u] * H + (size_t)c * 16);
+                sraw[u] = kMx ? (uint32_t)__ldg(static_cast<const uint8_t *>(yscale) + (size_t)p[u] * nb + sb)
+                              : __float_as_uint(__ldg(static_cast<const float *>(yscale) + (size_t)p[u] * nb + sb));
+            }
+#pragma unroll
+        for (int u = 0; u < kSlotBatch; ++u)
+            if (p[u] >= 0) {
+                const float sc = kMx ? e8m0_to_f32(sraw[u]) : __uint_as_float(sraw[u]);
+                const float ws = ww[u] * sc;
+                fma_codes16(f2_pack(ws, ws), v[u], acc);
+            }
+    }
+    uint4 o0, o1;
+    pack_acc16(acc, o0, o1);
+    uint16_t *dst = out + (size_t)t * H + (size_t)c * 16;
+    st_stream16(dst, o0);
+    st_stream16(dst + 8, o1);
+}
+
+// Launches a flat kernel with programmatic stream serialisation.
+template <class... P, class... A>
+cudaError_t launch_flat(void (*kern)(P...), long long threads, cudaStream_t st, A... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + kFlatThreads - 1) / kFlatThreads));
+    cfg.blockDim = dim3(kFlatThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // Few slots per token (k <= 2, Mixtral-like routing): one warp per token and
@@ -440,10 +596,10 @@ __global__ void __launch_bounds__(kFp8WarpThreads, 7) combine_fp8_warp_kernel(co
                 const int c = c0 + 32 * m;
                 if (c >= C16)
                     continue;
-                float acc[16];
+                uint64_t acc[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[i] = 0.0f;
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = 0ull;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int q = j == 0 ? q0 : q1;
@@ -452,27 +608,10 @@ __global__ void __launch_bounds__(kFp8WarpThreads, 7) combine_fp8_warp_kernel(co
                     const uint32_t sr = j == 0 ? s0[m] : s1[m];
                     const float sc = kMx ? e8m0_to_f32(sr) : __uint_as_float(sr);
                     const float ws = (j == 0 ? w0 : w1) * sc;
-                    const uint4 v = j == 0 ? v0[m] : v1[m];
-                    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float d0, d1, d2, d3;
-                        e4m3x4_to_f32(vv[i], d0, d1, d2, d3);
-                        acc[4 * i] = fmaf(ws, d0, acc[4 * i]);
-                        acc[4 * i + 1] = fmaf(ws, d1, acc[4 * i + 1]);
-                        acc[4 * i + 2] = fmaf(ws, d2, acc[4 * i + 2]);
-                        acc[4 * i + 3] = fmaf(ws, d3, acc[4 * i + 3]);
-                    }
+                    fma_codes16(f2_pack(ws, ws), j == 0 ? v0[m] : v1[m], acc);
                 }
                 uint4 o0, o1;
-                o0.x = pack_bf16x2(acc[0], acc[1]);
-                o0.y = pack_bf16x2(acc[2], acc[3]);
-                o0.z = pack_bf16x2(acc[4], acc[5]);
-                o0.w = pack_bf16x2(acc[6], acc[7]);
-                o1.x = pack_bf16x2(acc[8], acc[9]);
-                o1.y = pack_bf16x2(acc[10], acc[11]);
-                o1.z = pack_bf16x2(acc[12], acc[13]);
-                o1.w = pack_bf16x2(acc[14], acc[15]);
+                pack_acc16(acc, o0, o1);
                 uint16_t *dst = out + (size_t)t * H + (size_t)c * 16;
                 st_stream16(dst, o0);
                 st_stream16(dst + 8, o1);
@@ -500,6 +639,8 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
     }
     static PerDeviceCache<1> occ;  // the same registers either way: sized on the unsplit kernel
     const int per_sm = occupancy_per_sm(occ, (const void *)combine_kernel<false>, kCombThreads, 0);
+    if (T < device_sm_count() * per_sm)  // decode-sized: one thread per chunk
+        return launch_flat(combine_flat_kernel, (long long)T * (H / 8), st, y, pos, w, T, H, k, out, rows, err_flag);
     const int S = column_segments(T, H / 8, device_sm_count() * per_sm);
     long long grid = (long long)device_sm_count() * per_sm;
     if (grid > (long long)T * S)
@@ -540,6 +681,12 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
     const void *kern =
         mx ? (const void *)combine_fp8_kernel<true, false> : (const void *)combine_fp8_kernel<false, false>;
     const int per_sm = occupancy_per_sm(occ, kern, kCombThreads, 0, mx ? 1 : 0);
+    if (T < device_sm_count() * per_sm) {  // decode-sized: one thread per chunk
+        const long long n = (long long)T * (H / 16);
+        return mx ? launch_flat(combine_fp8_flat_kernel<true>, n, st, yq, yscale, pos, w, T, H, k, out, rows, err_flag)
+                  : launch_flat(combine_fp8_flat_kernel<false>, n, st, yq, yscale, pos, w, T, H, k, out, rows,
+                                err_flag);
+    }
     const int S = column_segments(T, H / 16, device_sm_count() * per_sm);
     long long gl = (long long)device_sm_count() * per_sm;
     if (gl > (long long)T * S)

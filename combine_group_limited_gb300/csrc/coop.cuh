@@ -1,5 +1,7 @@
-// coop.cuh -- helpers of the cooperative (grid-barrier) kernels: the fused
-// decode path and the fused gating + layout.  Not part of the public ABI.
+// coop.cuh -- helpers of the kernels whose CTAs work together: the bounded
+// grid barrier of the cooperative kernels, and the thread-block cluster
+// primitives (rank, barrier halves, distributed shared memory) of the
+// clustered ones.  Not part of the public ABI.
 #pragma once
 
 #include "ep_internal.cuh"
@@ -56,6 +58,60 @@ __device__ __forceinline__ bool grid_barrier(unsigned *word, unsigned expected, 
     __syncthreads();
     return s_ok != 0;
 }
+
+__device__ __forceinline__ unsigned cluster_ctarank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned cluster_nctarank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Index of this CTA's cluster in the (one-dimensional) grid of clusters.
+__device__ __forceinline__ unsigned cluster_id_x()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Cluster-wide barrier halves: arrive releases this thread's prior writes
+// (shared and global) to the cluster, wait acquires those of every thread
+// that arrived.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Generic address of `local`'s counterpart in the shared memory of cluster
+// CTA `rank`.
+template <class V>
+__device__ __forceinline__ const V *cluster_peer(const V *local, unsigned rank)
+{
+    uint64_t r;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+    return reinterpret_cast<const V *>(r);
+}
+
+// Stores v into `local`'s counterpart in the shared memory of cluster CTA
+// `rank` (a 32-bit shared::cluster address; no reply is awaited).
+__device__ __forceinline__ void cluster_store(int32_t *local, unsigned rank, int v)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on to
+// complete (no-op without the launch attribute), and let dependent grids
+// start their prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Inclusive warp scan.
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)

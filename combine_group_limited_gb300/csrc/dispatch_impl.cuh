@@ -151,20 +151,27 @@ __device__ __forceinline__ void load16(const uint16_t *__restrict__ xrow, int c,
     }
 }
 
-// fp8_quant16's arithmetic on 16 values already loaded by load16.
+// fp8_quant16's arithmetic on 16 values already loaded by load16.  The
+// values are unpacked negated (one xor flips both signs of a bf16 pair) so
+// that the quotient's three steps run as packed fp32x2 operations, whose
+// operands cannot be negated in place: x*r is formed as (-x)*(-r), and the
+// remainder and the correction take -x and -r; each product and sum is the
+// same exact value as in the scalar form, so every rounding -- and the sign
+// of a zero -- is the same.
 __device__ __forceinline__ uint4 fp8_quant16_regs(const uint4 &a, const uint4 &b, float &s_out)
 {
     const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float f[16];
+    float nf[16];  // -x
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16_lo(wv[i]);
-        f[2 * i + 1] = bf16_hi(wv[i]);
+        const uint32_t n = wv[i] ^ 0x80008000u;
+        nf[2 * i] = bf16_lo(n);
+        nf[2 * i + 1] = bf16_hi(n);
     }
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, fabsf(nf[i]));
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
@@ -192,23 +199,24 @@ __device__ __forceinline__ uint4 fp8_quant16_regs(const uint4 &a, const uint4 &b
         // remainder's sign convention (s*q0 - x, then q0 - e*r) keeps the
         // sign of a zero x.
         const float r = __frcp_rn(s);
+        const uint64_t s2 = f2_pack(s, s), nr2 = f2_pack(-r, -r);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float d[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float x = f[4 * i + j];
-                const float q0 = x * r;
-                const float e = fmaf(q0, s, -x);
-                d[j] = fmaf(-e, r, q0);
+            for (int j = 0; j < 4; j += 2) {
+                const uint64_t nx = f2_pack(nf[4 * i + j], nf[4 * i + j + 1]);
+                const uint64_t q0 = f2_mul(nx, nr2);   // x * r
+                const uint64_t e = f2_fma(q0, s2, nx);  // q0 * s - x, exact
+                f2_unpack(f2_fma(e, nr2, q0), d[j], d[j + 1]);  // q0 - e * r
             }
             q[i] = pack_e4m3x2(d[0], d[1]) | (pack_e4m3x2(d[2], d[3]) << 16);
         }
     } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
-            const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
+            const uint32_t lo = pack_e4m3x2(__fdiv_rn(-nf[4 * i], s), __fdiv_rn(-nf[4 * i + 1], s));
+            const uint32_t hi = pack_e4m3x2(__fdiv_rn(-nf[4 * i + 2], s), __fdiv_rn(-nf[4 * i + 3], s));
             q[i] = lo | (hi << 16);
         }
     }
@@ -232,9 +240,10 @@ __device__ __forceinline__ void q8_item_load(const uint16_t *__restrict__ x, int
 }
 
 // FP8 e4m3 with one fp32 scale per 128 columns: 8 lanes per block.  The
-// store half takes the item's values from q8_item_load.
-__device__ __forceinline__ void fp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a, const uint4 &b,
-                                               uint8_t *__restrict__ recv_q, float *__restrict__ recv_s)
+// store half takes the item's values from q8_item_load; fp8_item_put stores
+// codes and scale already computed by fp8_quant16_regs.
+__device__ __forceinline__ void fp8_item_put(int H, int k, int seg, int p0, int p1, const uint4 &qv, float s,
+                                             uint8_t *__restrict__ recv_q, float *__restrict__ recv_s)
 {
     const int lane = threadIdx.x & 31;
     const int C16 = H / 16;  // 16-column groups per row; 8 per 128-column block
@@ -242,8 +251,6 @@ __device__ __forceinline__ void fp8_item_store(int H, int k, int seg, int p0, in
     const int c = seg * 32 + lane;
     // C16 is a multiple of 8, so each 8-lane block is wholly in or out.
     const bool act = c < C16;
-    float s;
-    const uint4 qv = fp8_quant16_regs(a, b, s);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)
@@ -252,6 +259,14 @@ __device__ __forceinline__ void fp8_item_store(int H, int k, int seg, int p0, in
         if ((c & 7) == 0)
             recv_s[(size_t)p * nb + (c >> 3)] = s;
     }
+}
+
+__device__ __forceinline__ void fp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a, const uint4 &b,
+                                               uint8_t *__restrict__ recv_q, float *__restrict__ recv_s)
+{
+    float s;
+    const uint4 qv = fp8_quant16_regs(a, b, s);
+    fp8_item_put(H, k, seg, p0, p1, qv, s, recv_q, recv_s);
 }
 
 __device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x, int H, int k, long long t, int seg,
@@ -266,6 +281,8 @@ __device__ __forceinline__ void dispatch_fp8_item(const uint16_t *__restrict__ x
 // MXFP8 (E4M3 elements, E8M0 scale per 32 columns): the codes of the 16
 // columns [16c, 16c + 16) and their block's scale byte.  Two consecutive
 // lanes cover a block: every lane of the warp calls this.
+// The products x * 2^-e run as packed fp32x2 multiplies (the same IEEE
+// products, two per instruction).
 __device__ __forceinline__ uint4 mx_quant16_regs(const uint4 &a, const uint4 &b, uint8_t &e_out)
 {
     const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -286,12 +303,14 @@ __device__ __forceinline__ uint4 mx_quant16_regs(const uint4 &a, const uint4 &b,
     int e = ef == 0 ? -127 : ef - 127 - 8;
     e = e < -127 ? -127 : e;
     const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e in [-127, 119]
+    const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t q[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = pack_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
-        const uint32_t hi = pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-        q[i] = lo | (hi << 16);
+        float d[4];
+        f2_unpack(f2_mul(f2_pack(f[4 * i], f[4 * i + 1]), inv2), d[0], d[1]);
+        f2_unpack(f2_mul(f2_pack(f[4 * i + 2], f[4 * i + 3]), inv2), d[2], d[3]);
+        q[i] = pack_e4m3x2(d[0], d[1]) | (pack_e4m3x2(d[2], d[3]) << 16);
     }
     e_out = (uint8_t)(e + 127);
     return make_uint4(q[0], q[1], q[2], q[3]);
@@ -305,17 +324,15 @@ __device__ __forceinline__ uint4 mx_quant16(const uint16_t *__restrict__ xrow, i
 }
 
 // MXFP8: two lanes per 32-column block, E8M0 scale byte.  The store half
-// takes the item's values from q8_item_load.
-__device__ __forceinline__ void mxfp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a,
-                                                 const uint4 &b, uint8_t *__restrict__ recv_q,
-                                                 uint8_t *__restrict__ recv_e)
+// takes the item's values from q8_item_load; mxfp8_item_put stores codes and
+// scale byte already computed by mx_quant16_regs.
+__device__ __forceinline__ void mxfp8_item_put(int H, int k, int seg, int p0, int p1, const uint4 &qv, uint8_t eb,
+                                               uint8_t *__restrict__ recv_q, uint8_t *__restrict__ recv_e)
 {
     const int lane = threadIdx.x & 31;
     const int nb = H / 32;  // scale bytes per row
     const int c = seg * 32 + lane;
     const bool act = c < H / 16;  // H / 16 is even: lane pairs are wholly in or out
-    uint8_t eb;
-    const uint4 qv = mx_quant16_regs(a, b, eb);
     for (int j = 0; j < k; ++j) {
         const int p = slot_row(p0, p1, j);
         if (p < 0 || !act)
@@ -324,6 +341,15 @@ __device__ __forceinline__ void mxfp8_item_store(int H, int k, int seg, int p0, 
         if ((c & 1) == 0)
             recv_e[(size_t)p * nb + (c >> 1)] = eb;
     }
+}
+
+__device__ __forceinline__ void mxfp8_item_store(int H, int k, int seg, int p0, int p1, const uint4 &a,
+                                                 const uint4 &b, uint8_t *__restrict__ recv_q,
+                                                 uint8_t *__restrict__ recv_e)
+{
+    uint8_t eb;
+    const uint4 qv = mx_quant16_regs(a, b, eb);
+    mxfp8_item_put(H, k, seg, p0, p1, qv, eb, recv_q, recv_e);
 }
 
 __device__ __forceinline__ void dispatch_mxfp8_item(const uint16_t *__restrict__ x, int H, int k, long long t,

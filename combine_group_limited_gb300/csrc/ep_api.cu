@@ -190,7 +190,8 @@ ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, cons
     const ep::GateParams gp = gate_params(cfg);
     // The grid-wide launch with lane-segment gating for group-limited
     // batches past decode size and for batches past one cluster's layout;
-    // otherwise the gate kernel then the layout (one CTA, or one cluster).
+    // decode-sized batches in one clustered launch; otherwise the gate
+    // kernel then the layout (one CTA, or one cluster).
     const long long entries = (long long)T * k;
     const bool grouped = gp.Kg < gp.G;
     if (T > 0 && entries > ep::kSmallLayoutEntries && (grouped || entries > ep::kClusterLayoutEntries) &&
@@ -198,10 +199,15 @@ ep_status ep_gate_layout(const float *scores, const float *bias, int32_t T, cons
         return launched(ep::launch_route(scores, bias, &gp, nullptr, topk_idx, topk_w, T, k, E, experts_per_rank,
                                          expert_count, expert_off, rank_count, rank_off, rank_tokens, pos, src,
                                          err_flag, workspace, st));
-    // batches of at most 4096 entries (the gate kernel and the one-CTA
-    // layout: a grid-wide launch only adds latency there), configurations
-    // the lane-segment gating does not serve, and batches too large for one
-    // grid of one CTA per SM: the two steps' own kernels
+    // decode-sized batches (at most 4096 entries, 512 tokens): one
+    // clustered launch with no grid barrier
+    if (T > 0 && entries <= ep::kSmallLayoutEntries && ep::gate_layout_small_supported(T, k))
+        return launched(ep::launch_gate_layout_small(scores, bias, T, gp, experts_per_rank, topk_idx, topk_w,
+                                                     expert_count, expert_off, rank_count, rank_off, rank_tokens,
+                                                     pos, src, st));
+    // configurations the lane-segment gating does not serve, batches too
+    // large for one grid of one CTA per SM, and those between: the two
+    // steps' own kernels
     cudaError_t e = ep::launch_gate(scores, bias, T, gp, topk_idx, topk_w, st);
     if (e == cudaSuccess)
         e = ep::launch_layout(topk_idx, T, k, E, experts_per_rank, expert_count, expert_off, rank_count, rank_off,

@@ -44,6 +44,35 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
     return (uint32_t)r;
 }
 
+// Two fp32 values in one 64-bit register (low, high) for the packed fp32x2
+// arithmetic of sm_100-family GPUs: each lane of a packed op is the IEEE
+// round-to-nearest-even result of the scalar op, so packing changes no bit.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // 16-byte global load that bypasses L1 allocation (each byte is read once).
 __device__ __forceinline__ uint4 ld_stream16(const void *p)
 {
@@ -169,6 +198,14 @@ cudaError_t launch_decode(const float *scores, const float *bias, int T, const G
                           long long rows, int32_t *err_flag, void *barrier_word, cudaStream_t st);
 cudaError_t launch_barrier_selftest(unsigned extra, long long spin_limit, int32_t *err_flag, void *barrier_word,
                                     cudaStream_t st);
+// Gating and layout of a decode-sized batch (T <= 512, T*k <= 4096) in one
+// clustered launch with no grid barrier (decode.cu): results equal
+// launch_gate then launch_layout.
+bool gate_layout_small_supported(int T, int k);
+cudaError_t launch_gate_layout_small(const float *scores, const float *bias, int T, const GateParams &gp, int epr,
+                                     int32_t *topk_idx, float *topk_w, int32_t *expert_count, int32_t *expert_off,
+                                     int32_t *rank_count, int32_t *rank_off, int32_t *rank_tokens, int32_t *pos,
+                                     int32_t *src, cudaStream_t st);
 
 // Gating (gp != NULL: scores -> topk_idx, topk_w, with the lane-segment
 // body) and the layout of the chosen experts, or the layout of topk_idx_in

@@ -30,7 +30,7 @@ constexpr int kGateThreads = 256;
 constexpr int kGateWarps = kGateThreads / 32;
 
 template <int EPL>
-__global__ void __launch_bounds__(kGateThreads) gate_kernel(const float *__restrict__ scores,
+__global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const float *__restrict__ scores,
                                                             const float *__restrict__ bias, int T,
                                                             GateParams p, int group_lanes, int vec_rows,
                                                             int32_t *__restrict__ topk_idx,

@@ -65,12 +65,13 @@ __device__ __forceinline__ void sort_desc(uint32_t (&a)[N])
 }
 
 // Words of per-warp shared scratch gate_token needs: every lane's sorted
-// keys, then the chosen experts of the k slots.  (The general group path
-// also stages the row's keys there first: E <= 32 * EPL words.)
+// keys, then the chosen experts of the k slots, then their raw scores.
+// (The general group path also stages the row's keys there first: E <= 32 *
+// EPL words.)
 template <int EPL>
 __host__ __device__ constexpr int gate_warp_words()
 {
-    return 32 * EPL + 32;
+    return 32 * EPL + 64;
 }
 
 // Gates token t with the calling warp (all 32 lanes).  wsm: the warp's
@@ -88,41 +89,50 @@ __host__ __device__ constexpr int gate_warp_words()
 // finds each won key among its unsorted keys -- equal keys go lowest index
 // first, the order the tie rule asks for -- and writes the expert of that
 // round's slot.
+//
+// gate_token_slots leaves slot `lane`'s expert and weight in out_e and out_w
+// of lane lane < k; gate_token writes them to topk_idx and topk_w.
 template <int EPL>
-__device__ __forceinline__ void gate_token(const float *__restrict__ scores, const float *__restrict__ bias, int t,
-                                           const GateParams &p, int group_lanes, int vec_rows, uint32_t *wsm,
-                                           int32_t *__restrict__ topk_idx, float *__restrict__ topk_w)
+__device__ __forceinline__ void gate_token_slots(const float *__restrict__ scores, const float *__restrict__ bias,
+                                                 int t, const GateParams &p, int group_lanes, int vec_rows,
+                                                 uint32_t *wsm, int &out_e, float &out_w)
 {
     const int lane = threadIdx.x & 31;
     const int E = p.E;
     const int e0 = lane * EPL;
     const float *row = scores + (size_t)t * E;
 
-    float key[EPL];
+    // sc: the raw scores (kept for the weights, so that the row is read
+    // once); key: the selection keys score + bias
+    float sc[EPL], key[EPL];
     if (EPL % 4 == 0 && vec_rows) {
 #pragma unroll
         for (int i = 0; i < EPL; i += 4) {
             const float4 s4 = __ldg(reinterpret_cast<const float4 *>(row + e0 + i));
-            key[i] = s4.x;
-            key[i + 1] = s4.y;
-            key[i + 2] = s4.z;
-            key[i + 3] = s4.w;
+            sc[i] = s4.x;
+            sc[i + 1] = s4.y;
+            sc[i + 2] = s4.z;
+            sc[i + 3] = s4.w;
         }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            key[i] = sc[i];
         if (bias) {
 #pragma unroll
             for (int i = 0; i < EPL; i += 4) {
                 const float4 b4 = __ldg(reinterpret_cast<const float4 *>(bias + e0 + i));
-                key[i] = key[i] + b4.x;
-                key[i + 1] = key[i + 1] + b4.y;
-                key[i + 2] = key[i + 2] + b4.z;
-                key[i + 3] = key[i + 3] + b4.w;
+                key[i] = sc[i] + b4.x;
+                key[i + 1] = sc[i + 1] + b4.y;
+                key[i + 2] = sc[i + 2] + b4.z;
+                key[i + 3] = sc[i + 3] + b4.w;
             }
         }
     } else {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = e0 + i;
-            key[i] = e < E ? (bias ? __ldg(row + e) + __ldg(bias + e) : __ldg(row + e)) : -INFINITY;
+            sc[i] = e < E ? __ldg(row + e) : 0.0f;
+            key[i] = e < E ? (bias ? sc[i] + __ldg(bias + e) : sc[i]) : -INFINITY;
         }
     }
     uint32_t ord[EPL];
@@ -236,6 +246,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
     // This lane's sorted keys, for the rounds to read past the head.
     uint32_t *lst = wsm + lane * EPL;
     int32_t *s_e = reinterpret_cast<int32_t *>(wsm + 32 * EPL);
+    float *s_raw = reinterpret_cast<float *>(wsm + 32 * EPL + 32);
     if (EPL % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < EPL; i += 4)
@@ -245,7 +256,9 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
         for (int i = 0; i < EPL; ++i)
             lst[i] = srt[i];
     }
-    s_e[lane] = 0;  // a slot no round fills (impossible for finite scores) stays in range
+    // a slot no round fills (impossible for finite scores) names expert 0
+    s_e[lane] = 0;
+    s_raw[lane] = __shfl_sync(kFullMask, sc[0], 0);
     __syncwarp();
 
     // Top-k rounds over the lanes' heads.
@@ -279,19 +292,25 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
             m &= ~used;
             const int i = __ffs(m) - 1;
             used |= 1u << i;
+            float v = sc[0];
+#pragma unroll
+            for (int ii = 1; ii < EPL; ++ii)
+                v = ii == i ? sc[ii] : v;
             s_e[j] = e0 + i;
+            s_raw[j] = v;
         }
     }
     __syncwarp();
     int my_e = 0;
+    float my_s = 0.0f;  // the unbiased score of slot `lane`
     if (lane < k) {
         const int e = s_e[lane];
         my_e = (unsigned)e < (unsigned)E ? e : 0;
+        my_s = s_raw[lane];
     }
     __syncwarp();  // the scratch may be reused by the warp's next token
 
     // Weights from the unbiased score, sums taken in slot order.
-    const float my_s = (lane < k) ? __ldg(row + my_e) : 0.0f;
     float w;
     if (p.score_fn == 0) {
         if (p.normalize) {
@@ -318,7 +337,7 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
         float raw[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            raw[i] = (e0 + i < E) ? __ldg(row + e0 + i) : 0.0f;
+            raw[i] = (e0 + i < E) ? sc[i] : 0.0f;
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
@@ -337,9 +356,22 @@ __device__ __forceinline__ void gate_token(const float *__restrict__ scores, con
             z += __shfl_xor_sync(kFullMask, z, off);
         w = expf(my_s - m) / z;
     }
-    if (lane < k) {
-        topk_idx[(size_t)t * k + lane] = my_e;
-        topk_w[(size_t)t * k + lane] = w;
+    out_e = my_e;
+    out_w = w;
+}
+
+template <int EPL>
+__device__ __forceinline__ void gate_token(const float *__restrict__ scores, const float *__restrict__ bias, int t,
+                                           const GateParams &p, int group_lanes, int vec_rows, uint32_t *wsm,
+                                           int32_t *__restrict__ topk_idx, float *__restrict__ topk_w)
+{
+    int e;
+    float w;
+    gate_token_slots<EPL>(scores, bias, t, p, group_lanes, vec_rows, wsm, e, w);
+    const int lane = threadIdx.x & 31;
+    if (lane < p.k) {
+        topk_idx[(size_t)t * p.k + lane] = e;
+        topk_w[(size_t)t * p.k + lane] = w;
     }
 }
 

@@ -27,7 +27,7 @@
 // shared memory) may overlap the previous kernel; griddepcontrol.wait comes
 // before any global memory access.  Results equal the other layout paths'
 // bit for bit.
-#include "ep_internal.cuh"
+#include "coop.cuh"
 
 namespace ep {
 
@@ -48,34 +48,6 @@ struct LcArgs {
     int32_t *expert_count, *expert_off, *rank_count, *rank_off, *rank_tokens, *expert_dropped, *pos, *src;
     int32_t *err_flag;
 };
-
-__device__ __forceinline__ unsigned cluster_ctarank()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ unsigned cluster_nctarank()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// Cluster-wide barrier halves: arrive releases this thread's prior writes
-// (shared and global) to the cluster, wait acquires everyone else's.
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-// Generic address of `local`'s counterpart in the shared memory of cluster
-// CTA `rank`.
-__device__ __forceinline__ const int32_t *cluster_peer(const int32_t *local, unsigned rank)
-{
-    uint64_t r;
-    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
-    return reinterpret_cast<const int32_t *>(r);
-}
 
 __device__ __forceinline__ int warp_incl_sum(int v, int lane)
 {

@@ -76,34 +76,6 @@ __host__ __device__ inline int route_phases(int E4)
     return q;
 }
 
-__device__ __forceinline__ unsigned cluster_ctarank()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ unsigned cluster_nctarank()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// Cluster-wide barrier halves: arrive releases this thread's prior writes
-// to the cluster, wait acquires those of every thread that arrived.
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-// Generic address of `local`'s counterpart in the shared memory of cluster
-// CTA `rank`.
-__device__ __forceinline__ const int32_t *cluster_peer(const int32_t *local, unsigned rank)
-{
-    uint64_t r;
-    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
-    return reinterpret_cast<const int32_t *>(r);
-}
-
 // Shared-memory words: [gating: bias rows (floats), candidate lists (2 words
 // each), chosen experts and scores], then, 16-byte aligned, [layout: this
 // CTA's totals, pre, totals (all three take 16-byte accesses), distinct

@@ -159,13 +159,16 @@ ep_status ep_get_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E
  * Steps 1 and 2 in one call: ep_gate, then ep_get_layout of the experts it
  * chose, with the outputs of those two calls bit for bit ("DeepEP de DeepSeek
  * ...", section "Group-limited gating algorithm"; "Expert Parallelism ...",
- * section "Le principe de base").  Each is short and latency-bound at full
- * batch size; here, while a grid of one CTA per SM covers the batch with at
- * most 4096 entries per CTA, both run in one cooperative launch whose CTAs
- * gate and count their own tokens, meet at one grid barrier and then place
- * them.  Batches of at most 4096 entries (T*k), where one CTA lays out the
- * whole batch and a grid-wide launch only adds latency, and batches too large
- * for that grid run the two calls' own kernels.
+ * section "Le principe de base").  Each is short and latency-bound.  Which
+ * kernels run depends on the batch:
+ *  - at most 4096 entries (T*k) and 512 tokens (decode-sized): one launch
+ *    of one thread-block cluster, whose CTAs gate a slice of the tokens each
+ *    and exchange per-expert token masks through distributed shared memory;
+ *  - group-limited gating past that, and any gating past 65536 entries,
+ *    while a grid of one CTA per SM covers the batch with at most 128
+ *    tokens per CTA: one cooperative launch whose CTAs gate and count their
+ *    own tokens, meet at one grid barrier and then place them;
+ *  - otherwise the two calls' own kernels.
  *
  * Arguments: those of ep_gate (scores, bias, T, cfg, topk_idx, topk_w) and
  * of ep_get_layout (experts_per_rank, expert_count .. src, err_flag), with
@@ -338,8 +341,13 @@ ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_row
  * Fused low-latency path for decode-sized batches ("DeepEP de DeepSeek
  * ...", section "Kernels low-latency dispatch et combine"; "Expert
  * Parallelism ...": decode messages of 100 KB - 2 MB): ep_gate,
- * ep_get_layout and ep_dispatch in ONE cooperative launch, with results
- * identical to the three separate calls.
+ * ep_get_layout and ep_dispatch in ONE launch, with results identical to
+ * the three separate calls.  Up to 512 tokens the launch is a grid of
+ * thread-block clusters with no grid barrier: every cluster gates and lays
+ * out the whole batch (its CTAs exchange per-expert token masks through
+ * distributed shared memory) and scatters its share of the tokens.  Larger
+ * batches take one cooperative launch with a grid barrier between gating
+ * and layout.
  *
  * Arguments as those calls (cfg as ep_gate; experts_per_rank and the layout
  * outputs as ep_get_layout; x, H, dtype, recv, recv_rows, recv_scales as
@@ -348,7 +356,7 @@ ep_status ep_combine_backward(const void *grad_out, const void *y, int32_t y_row
  * 4-byte aligned, whose first 4 bytes hold the grid barrier's arrival count:
  * zero it once before the first call; each call leaves it zero for the
  * next (calls sharing it must not overlap on the GPU).  The grid barrier
- * between gating and layout waits at most about a second; if that ran out,
+ * (batches past 512 tokens) waits at most about a second; if that ran out,
  * EP_FLAG_TIMEOUT is set in *err_flag, the outputs are incomplete and the
  * workspace must be zeroed again.
  * A device without cooperative launch returns EP_ERR_CUDA.

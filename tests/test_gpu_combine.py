@@ -97,3 +97,25 @@ def test_combine_all_slots_empty_gives_zero(ep):
     g, _ = _combine_both(ep, synth.f32_to_bf16_bits(np.ones((8, 64), np.float32)), pos, np.ones((2, 4), np.float32))
     assert np.all(g == 0)
     del y
+
+
+@pytest.mark.parametrize("k,unit", [(8, False), (2, False), (8, True)])
+def test_combine_decode_sized_batch_equals_rows_of_a_large_batch(ep, k, unit):
+    """A batch with fewer tokens than resident CTAs takes the thread-per-chunk
+    kernel, a large one the CTA kernels: the same fp32 fma chain in slot
+    order, so the small batch's rows equal the large batch's bit for bit
+    (unit weights: the dispatch backward)."""
+    rng = np.random.default_rng(40 + k)
+    T, H = 3000, 1024
+    y = synth.f32_to_bf16_bits(rng.normal(0, 1, (T * k, H)).astype(np.float32))
+    pos = rng.permutation(T * k).reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.1] = -1
+    w = None if unit else dev(rng.uniform(-1, 1, (T, k)).astype(np.float32))
+    yd, pd = dev_bf16(y), dev(pos)
+    big = ep.ep_combine(yd, pd, w) if not unit else ep.ep_dispatch_backward(yd, pd)
+    n = 100
+    small = (ep.ep_combine(yd, pd[:n].contiguous(), w[:n].contiguous()) if not unit
+             else ep.ep_dispatch_backward(yd, pd[:n].contiguous()))
+    torch.cuda.synchronize()
+    assert torch.equal(small, big[:n])
+

@@ -1,6 +1,7 @@
 """GPU parity of the fused low-latency decode path (gate + layout + dispatch
-in one launch) against the CPU oracle and against the separate calls, and
-the bounded grid barrier's timeout path."""
+in one launch: the clustered kernel up to 512 tokens, the cooperative one
+past that) against the CPU oracle and against the separate calls, and the
+bounded grid barrier's timeout path."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +26,8 @@ def ep():
     ("decode", 128, "bf16"), ("decode", 128, "fp8"), ("decode", 128, "mxfp8"), ("decode", 1, "bf16"),
     ("decode", 77, "fp8"), ("dsv3", 256, "fp8"), ("dsv3", 512, "bf16"), ("skewed", 300, "mxfp8"),
     ("tiny", 128, "bf16"), ("mixtral", 2048, "bf16"), ("qwen3", 64, "bf16"),
+    ("decode", 2, "fp8"), ("decode", 9, "mxfp8"), ("qwen3", 512, "bf16"), ("tiny", 600, "fp8"),
+    ("mixtral", 513, "bf16"),
 ])
 def test_decode_fused_matches_oracle(ep, name, T, dtype):
     cfg = synth.config(name, T=T)

@@ -101,3 +101,26 @@ def test_gate_small_token_counts(ep, T):
         oi, ow = oracle.gate(scores, bias, *gate_args(cfg))
         np.testing.assert_array_equal(gi, oi)
         assert_weights_close(gw, ow, weight_rtol(cfg, scores, oi))
+
+
+@pytest.mark.parametrize("E,G,Kg,kin,k", [(256, 1, 1, 1, 8), (256, 8, 4, 2, 8), (64, 1, 1, 1, 4), (8, 1, 1, 1, 2)])
+def test_gate_planted_ties_at_and_inside_the_top_k(ep, E, G, Kg, kin, k):
+    """Distinct random keys except where planted: one third of the tokens
+    get a key equal to their k-th largest just outside the top k (the lower
+    index must win the last slot), one third two equal keys inside the top
+    k (lower index first), the rest none -- the warp's merged top-k path
+    serves the last third, the round-by-round path the others."""
+    rng = np.random.default_rng(E + k)
+    T = 66
+    scores = rng.normal(0, 1, size=(T, E)).astype(np.float32)
+    for t in range(T):
+        order = np.argsort(-scores[t], kind="stable")
+        if t % 3 == 0 and k < E:
+            a, b = sorted((order[k - 1], order[k]))
+            scores[t, b] = scores[t, a]         # the k-th key, twice
+        elif t % 3 == 1 and k > 1:
+            scores[t, order[1]] = scores[t, order[0]]
+    cfg = dict(k=k, n_groups=G, topk_group=Kg, topk_in_group=kin, score_fn=synth.SCORE_RAW, normalize=True, E=E)
+    _check(ep, cfg, scores, None)
+    cfg["score_fn"] = synth.SCORE_SOFTMAX
+    _check(ep, cfg, scores, None)

@@ -139,6 +139,40 @@ def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset)
     _assert_fp8_combine_close(host_bits(out), r, _dequant(q, s, 128 if fmt == "fp8" else 32), pos, w)
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "mxfp8"])
+def test_combine_fp8_decode_sized_batch_equals_rows_of_a_large_batch(ep, fmt):
+    """Fewer tokens than resident CTAs: the thread-per-chunk kernel; its rows
+    equal the CTA kernel's on the same expert outputs bit for bit; a row
+    outside the buffer is flagged and skipped."""
+    rng = np.random.default_rng(71)
+    T, H, k = 3000, 1024, 8
+    rows = T * k
+    q = rng.integers(0, 256, size=(rows, H)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3C
+    s = (rng.uniform(0.01, 3, (rows, H // 128)).astype(np.float32) if fmt == "fp8"
+         else rng.integers(110, 140, (rows, H // 32)).astype(np.uint8))
+    pos = rng.permutation(rows).reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.1] = -1
+    w = rng.uniform(-1, 1, (T, k)).astype(np.float32)
+    qd, sd, pd, wd = dev(q), dev(s), dev(pos), dev(w)
+    big = ep.ep_combine_fp8(qd, sd, pd, wd)
+    n = 100
+    small = ep.ep_combine_fp8(qd, sd, pd[:n].contiguous(), wd[:n].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(small, big[:n])
+    bad = pos[:n].copy()
+    bad[3, 2] = rows + 5
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = ep.ep_combine_fp8(qd, sd, dev(bad), wd[:n].contiguous(), err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 2
+    skip = pos[:n].copy()
+    skip[3, 2] = -1
+    want = ep.ep_combine_fp8(qd, sd, dev(skip), wd[:n].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+
+
 # -------------------------------------------------------- capacity layout
 
 CAP_KEYS = ("expert_count", "expert_off", "rank_count", "rank_off", "rank_tokens", "expert_dropped", "pos", "src")

@@ -1,4 +1,5 @@
-"""GPU parity of the routing call ep_gate_layout (one grid-wide launch for
+"""GPU parity of the routing call ep_gate_layout (one clustered launch for
+batches of at most 4096 entries and 512 tokens; one grid-wide launch for
 group-limited batches past 4096 entries and for batches past 65536 entries;
 the gate kernel then the one-CTA or one-cluster layout otherwise) and of
 ep_get_layout past 4096 entries (one cluster, the grid-wide launch, or three
@@ -31,7 +32,8 @@ def _check_layout(lay, ol):
 
 
 @pytest.mark.parametrize("name,T", [(n, None) for n in synth.CONFIGS] + [
-    ("dsv3", 1), ("dsv3", 151), ("dsv3", 152), ("dsv3", 153), ("dsv3", 1000), ("skewed", 3001),
+    ("dsv3", 1), ("dsv3", 2), ("dsv3", 9), ("dsv3", 151), ("dsv3", 152), ("dsv3", 153), ("dsv3", 512),
+    ("qwen3", 300), ("mixtral", 512), ("mixtral", 513), ("tiny", 1000), ("dsv3", 1000), ("skewed", 3001),
     ("qwen3", 40000), ("mixtral", 70001), ("dsv3", 100003),
 ])
 def test_gate_layout_matches_oracle_and_separate_calls(ep, name, T):
