@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import random
 import statistics
 import subprocess
 import sys
@@ -40,6 +41,20 @@ WORKLOAD = "dsv3"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20          # twice the 129 MB L2
 QUEUE_AHEAD_CYCLES = 200_000        # ~0.1 ms of GPU spin before each timed step (host launches get ahead)
+# The CUDA event clock ticks in steps of about 2 us on this GPU, and a fixed
+# spin before each timed call starts it at the same phase of a tick every
+# time, so every repetition rounds the same way.  A random extra spin of up
+# to ~4 us (two ticks) spreads the phase: the mean over repetitions then
+# resolves below a tick.
+DITHER_CYCLES = 8192
+_dither = random.Random(20261203)
+
+
+def queue_ahead():
+    """The spin before a timed call (outside the events): queue-ahead plus
+    a random phase."""
+    import torch
+    torch.cuda._sleep(QUEUE_AHEAD_CYCLES + _dither.randrange(DITHER_CYCLES))
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -360,11 +375,18 @@ CONFIG_RUNS = {
 }
 
 
+def trimmed_mean(ts, cut=0.05):
+    """Mean of the values between the `cut` and 1 - `cut` quantiles."""
+    v = sorted(ts)
+    n = int(len(v) * cut)
+    return statistics.mean(v[n:len(v) - n] if len(v) > 2 * n else v)
+
+
 def time_configs(reps, peak, flush_l2):
-    """Per workload: mean, median, p10 and p90 event times of each op over
-    `reps` L2-flushed calls, GB/s and fraction of the HBM peak from its
-    algorithmic bytes and the mean time, and the tokens/s of one routing +
-    dispatch + combine step (means)."""
+    """Per workload: mean (of the central 90 %), median, p10 and p90 event
+    times of each op over `reps` L2-flushed calls, GB/s and fraction of the
+    HBM peak from its algorithmic bytes and the mean time, and the tokens/s
+    of one routing + dispatch + combine step (means)."""
     import torch
     stream = torch.cuda.current_stream()
     out = {}
@@ -391,9 +413,10 @@ def time_configs(reps, peak, flush_l2):
                 if i >= 2:
                     ts.append(a.elapsed_time(b) * 1e3)
             # The event clock ticks in steps of about 2 us on this GPU: the
-            # mean over the repetitions (random phase) resolves below a tick
-            # and gives the rates; the percentiles show the spread.
-            mean = statistics.mean(ts)
+            # mean over the repetitions (random phase, queue_ahead) resolves
+            # below a tick and gives the rates; the percentiles show the
+            # spread.
+            mean = trimmed_mean(ts)
             gbs = nbytes / (mean * 1e-6) / 1e9
             res[op] = {"us": round(mean, 2), "us_median": round(pct(ts, 50), 2), "us_p10": round(pct(ts, 10), 2),
                        "us_p90": round(pct(ts, 90), 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
@@ -437,7 +460,7 @@ def run_ours(args):
         # launch calls.
         flush.fill_(s & 0xFF)
         flush_rd.sum()
-        torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
+        queue_ahead()
 
     ops = ("route", "dispatch", "combine")
 
@@ -724,7 +747,7 @@ def run_sweep(args):
         for i in range(reps + 3):
             flush.fill_(i & 0xFF)
             flush_rd.sum()
-            torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
+            queue_ahead()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -734,8 +757,9 @@ def run_sweep(args):
                 ts.append(a.elapsed_time(b) * 1e3)
         # the event clock ticks in steps of about 2 us here: the mean over
         # many repetitions (random phase) resolves below a tick, a median
-        # does not
-        return statistics.mean(ts)
+        # does not; the slowest and fastest 5 % are left out (a host stall
+        # can hold one repetition for milliseconds)
+        return trimmed_mean(ts)
 
     def hot(fn, per_graph=20, replays=20):
         """Back-to-back calls replayed from a CUDA graph, no flush between
@@ -801,6 +825,9 @@ def run_sweep(args):
             ops["decode_fused"] = lambda: ep.ep_decode_dispatch(
                 r.scores, r.bias, gc, epr, r.x, "fp8", topk_idx=r.topk_idx, topk_w=r.topk_w, out=r.lay,
                 recv=r.recv_q, recv_scales=r.recv_s, workspace=dws)
+        if args.ops:  # a subset (e.g. one kernel under a profiler), in the same order
+            keep = set(args.ops.split(","))
+            ops = {n: f for n, f in ops.items() if n in keep}
         # run every op once so that its inputs exist (mxfp8 codes for its combine)
         for fn in ops.values():
             fn()
@@ -811,13 +838,15 @@ def run_sweep(args):
             us = timed(fn, args.reps)
             gbs = nb[op] / (us * 1e-6) / 1e9
             res[op] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb[op]}
-            if T * k <= 8192:                           # small enough to be latency-bound
+            if T * k <= 8192 and not args.no_hot:       # small enough to be latency-bound
                 h = hot(fn)
                 res[op]["hot_us"] = None if h is None else round(h, 3)
         dsp = "dispatch_fp8" if H % 128 == 0 else "dispatch_bf16"
-        step = lambda: (r.route(), ops[dsp](), r.combine())  # noqa: E731
-        step_us = timed(step, args.reps)
-        if "decode_fused" in ops:
+        step_us = float("nan")
+        if dsp in ops:
+            step = lambda: (r.route(), ops[dsp](), r.combine())  # noqa: E731
+            step_us = timed(step, args.reps)
+        if "decode_fused" in ops and not args.ops:
             sep = lambda: (r.gate(), r.layout(), r.dispatch())  # noqa: E731
             h = hot(sep)
             res["decode_separate"] = {"us": round(timed(sep, args.reps), 2),
@@ -838,6 +867,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--sweep", action="store_true", help="time every op on every workload (one line each)")
     ap.add_argument("--configs", default="", help="comma-separated workloads for --sweep")
+    ap.add_argument("--ops", default="", help="comma-separated ops for --sweep (default: all)")
+    ap.add_argument("--no-hot", action="store_true", help="--sweep: skip the graph-replayed back-to-back timing")
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="token chunks the end-to-end leg pipelines its copies and kernels over")
     ap.add_argument("--e2e-no-graph", action="store_true",

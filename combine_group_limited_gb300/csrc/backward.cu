@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(kBwdWarpThreads, 8) combine_backward_warp_kern
     long long rows, int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);  // grid <= T/4 + 1 blocks
-    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int warp = (int)balanced_warp();  // grid <= T blocks
+    const int nwarps = (int)grid_warps();
     const int C = H / 8;
     int np = -1;
     float nw = 0.0f;
@@ -297,10 +297,9 @@ cudaError_t launch_combine_backward(const uint16_t *grad_out, const uint16_t *y,
     if (k <= 2 && T >= 2048) {
         static PerDeviceCache<1> occ;
         const int per_sm = occupancy_per_sm(occ, (const void *)combine_backward_warp_kernel, kBwdWarpThreads, 0);
-        const long long need = ((long long)T + kBwdWarpThreads / 32 - 1) / (kBwdWarpThreads / 32);
-        long long g = (long long)device_sm_count() * per_sm;
-        if (g > need)
-            g = need;
+        long long g = (long long)device_sm_count() * per_sm;  // one token per CTA at least (balanced_warp)
+        if (g > T)
+            g = T;
         combine_backward_warp_kernel<<<(int)g, kBwdWarpThreads, 0, st>>>(grad_out, y, pos, w, T, H, k, grad_y,
                                                                           grad_w, rows, err_flag);
         return cudaGetLastError();

@@ -455,8 +455,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_warp_kernel(const uint16
                                                                     int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long warp = balanced_warp();
+    const long long nwarps = grid_warps();
     const int C = H / 8;
     // lane j < k holds slot j's row and weight (k <= 2)
     int np = -1;
@@ -546,8 +546,8 @@ __global__ void __launch_bounds__(kFp8WarpThreads, 7) combine_fp8_warp_kernel(co
                                                                         int32_t *__restrict__ err_flag)
 {
     const int lane = threadIdx.x & 31;
-    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long warp = balanced_warp();
+    const long long nwarps = grid_warps();
     const int C16 = H / 16;
     const int nb = kMx ? H / 32 : H / 128;
     int np = -1;
@@ -630,10 +630,9 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
     if (k <= 2 && T >= 2048) {
         static PerDeviceCache<1> occ;
         const int wps = occupancy_per_sm(occ, (const void *)combine_warp_kernel, kCombThreads, 0);
-        const long long need = ((long long)T + kCombThreads / 32 - 1) / (kCombThreads / 32);
-        long long g = (long long)device_sm_count() * wps;
-        if (g > need)
-            g = need;
+        long long g = (long long)device_sm_count() * wps;  // one token per CTA at least (balanced_warp)
+        if (g > T)
+            g = T;
         combine_warp_kernel<<<(int)g, kCombThreads, 0, st>>>(y, pos, w, T, H, k, out, rows, err_flag);
         return cudaGetLastError();
     }
@@ -665,10 +664,9 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
         static PerDeviceCache<2> occ;
         const void *wk = mx ? (const void *)combine_fp8_warp_kernel<true> : (const void *)combine_fp8_warp_kernel<false>;
         const int ps = occupancy_per_sm(occ, wk, kFp8WarpThreads, 0, mx ? 1 : 0);
-        const long long need = ((long long)T + kFp8WarpThreads / 32 - 1) / (kFp8WarpThreads / 32);
-        long long g = (long long)device_sm_count() * ps;
-        if (g > need)
-            g = need;
+        long long g = (long long)device_sm_count() * ps;  // one token per CTA at least (balanced_warp)
+        if (g > T)
+            g = T;
         if (mx)
             combine_fp8_warp_kernel<true><<<(int)g, kFp8WarpThreads, 0, st>>>(yq, yscale, pos, w, T, H, k, out, rows,
                                                                           err_flag);

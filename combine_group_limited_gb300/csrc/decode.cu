@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
 // Clustered decode path: no grid barrier.
 //
 // The gating and the layout of a decode batch are small next to its
-// dispatch, so every cluster of CS CTAs computes both for the WHOLE batch
+// dispatch, so every cluster of CS = 8 CTAs computes both for the WHOLE batch
 // (CTA r of a cluster gates tokens [T*r/CS, T*(r+1)/CS), one warp per
 // token), and the clusters then share the dispatch: of CTA r's warp items
 // (its tokens' row segments, in order), cluster c scatters items c, c + G,
@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_fused_kernel(const DecodeA
 // the previous kernel; griddepcontrol.wait precedes every global access.
 constexpr int kDcMaxTpc = 64;  // tokens per CTA: one bit each in a 64-bit mask
 constexpr int kDcMaxCluster = 8;
+constexpr int kDcMaxTokens = kDcMaxCluster * kDcMaxTpc;
 
 struct DcSmem {
     size_t gate, e, w, mask, rmask, cnt, rcnt, pre, off, total;
@@ -324,7 +325,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const De
     const int E = a.gp.E, k = a.gp.k, T = a.T, R = E / a.epr;
     const unsigned cs = cluster_nctarank(), cr = cluster_ctarank();
     const int cid = (int)cluster_id_x(), G = (int)(gridDim.x / cs);
-    const int t_lo = (int)((long long)T * cr / cs), t_hi = (int)((long long)T * (cr + 1) / cs);
+    // T <= 512 and cs <= 8: 32-bit products and divisions
+    const int t_lo = T * (int)cr / (int)cs, t_hi = T * ((int)cr + 1) / (int)cs;
     const int n_loc = t_hi - t_lo;
     const int tpc = (T + (int)cs - 1) / (int)cs;
     const DcSmem L = dc_smem(tpc, k, E, R, (int)cs, gate_warp_words<EPL>());
@@ -548,29 +550,30 @@ cudaError_t launch_cluster_epl(DecodeArgs a, cudaStream_t st)
 {
     int warp_floats;
     gate_plan<EPL>(a.gp, a.scores, a.bias, a.group_lanes, a.vec_rows, warp_floats);
-    const int cs = a.T < kDcMaxCluster ? a.T : kDcMaxCluster;
-    const int tpc = (a.T + cs - 1) / cs;
-    const size_t smem = dc_smem(tpc, a.gp.k, a.gp.E, a.gp.E / a.epr, cs, warp_floats).total;
-    if (smem > kDcMaxSmem)
-        return cudaErrorInvalidConfiguration;
     const void *fn = (const void *)decode_cluster_kernel<EPL>;
     static PerDeviceCache<1> smem_attr;
     const cudaError_t e = raise_smem_limit(smem_attr, fn, kDcMaxSmem);
     if (e != cudaSuccess)
         return e;
+    const int cs = a.T < kDcMaxCluster ? a.T : kDcMaxCluster;
+    const int tpc = (a.T + cs - 1) / cs;
+    const size_t smem = dc_smem(tpc, a.gp.k, a.gp.E, a.gp.E / a.epr, cs, warp_floats).total;
+    if (smem > kDcMaxSmem)
+        return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // clusters: about one row segment per warp, and no more than are
-    // resident at once (a cluster that waits for another to finish doubles
-    // the latency); one cluster when nothing is dispatched
+    // clusters: as many as are resident at once (a cluster that waits for
+    // another to finish doubles the latency; fewer leave SMs idle while the
+    // rows are written), at most one per row segment of a CTA; one cluster
+    // when nothing is dispatched
     int G = 1;
     if (a.dtype >= 0) {
         const int segs = a.dtype == 0 ? bf16_segs(a.H) : fp8_segs(a.H);
-        G = (tpc * segs + kDecWarps - 1) / kDecWarps;
+        G = tpc * segs;
         static PerDeviceCache<kDcMaxCluster + 1> resident;
         const int most = resident.get(
             [&] {
@@ -608,7 +611,7 @@ cudaError_t launch_cluster_epl(DecodeArgs a, cudaStream_t st)
 template <int EPL>
 cudaError_t launch_args(DecodeArgs a, cudaStream_t st)
 {
-    if (a.T <= kDcMaxCluster * kDcMaxTpc) {
+    if (a.T <= kDcMaxTokens) {
         const cudaError_t e = launch_cluster_epl<EPL>(a, st);
         if (e == cudaSuccess || a.dtype < 0)
             return e;
@@ -637,7 +640,7 @@ cudaError_t launch_by_experts(const DecodeArgs &a, cudaStream_t st)
 
 size_t decode_max_entries() { return kMaxEntries; }
 
-bool gate_layout_small_supported(int T, int k) { return T >= 1 && T <= kDcMaxCluster * kDcMaxTpc && (long long)T * k <= kMaxEntries; }
+bool gate_layout_small_supported(int T, int k) { return T >= 1 && T <= kDcMaxTokens && (long long)T * k <= kMaxEntries; }
 
 cudaError_t launch_gate_layout_small(const float *scores, const float *bias, int T, const GateParams &gp, int epr,
                                      int32_t *topk_idx, float *topk_w, int32_t *expert_count, int32_t *expert_off,

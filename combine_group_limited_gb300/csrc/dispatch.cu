@@ -107,6 +107,87 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_fp8_kernel(const uint16
     }
 }
 
+// FP8 / MXFP8 for few slots per token (k <= kQ8RowMaxK, Mixtral-like
+// routing): a warp walks whole tokens, their row segments in order, so a
+// token's receive rows are loaded and shuffled to the lanes once (kept in
+// registers) rather than once per segment, and the segment loop carries no
+// token bookkeeping; the next segment's row load (and at a token's last
+// segment, the next token's pos) is issued before the current one is
+// converted and stored.  The same per-segment arithmetic as the item
+// kernels (fp8_quant16_regs, mx_quant16_regs).
+constexpr int kQ8RowMaxK = 4;
+
+template <bool kMx>
+__global__ void __launch_bounds__(kDispThreads) dispatch_q8_rows_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                                        int k, const int32_t *__restrict__ pos,
+                                                                        uint8_t *__restrict__ recv_q,
+                                                                        void *__restrict__ recv_sc, long long rows,
+                                                                        int32_t *__restrict__ err_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const long long nw = grid_warps();
+    long long t = balanced_warp();
+    if (t >= T)
+        return;
+    const int segs = fp8_segs(H);
+    const int C16 = H / 16;
+    const int nb = kMx ? H / 32 : H / 128;
+    int pl = lane < k ? __ldg(pos + t * k + lane) : -1;  // slot `lane`'s row, as loaded
+    int seg = 0;
+    uint4 a, b;
+    q8_item_load(x, H, t, 0, a, b);
+    for (;;) {
+        // this token's rows, checked, in every lane
+        int p[kQ8RowMaxK];
+        if (pl >= rows) {
+            if (err_flag)
+                atomicOr(err_flag, 2);
+            pl = -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kQ8RowMaxK; ++j)
+            p[j] = __shfl_sync(kFullMask, pl, j);
+        for (;;) {
+            const bool last_seg = seg + 1 == segs;
+            const long long tn = last_seg ? t + nw : t;
+            const int sn = last_seg ? 0 : seg + 1;
+            const bool more = tn < T;  // warp-uniform
+            uint4 na = make_uint4(0, 0, 0, 0), nb4 = make_uint4(0, 0, 0, 0);
+            if (more)
+                q8_item_load(x, H, tn, sn, na, nb4);
+            if (more && last_seg)
+                pl = lane < k ? __ldg(pos + tn * k + lane) : -1;
+            const int c = seg * 32 + lane;
+            const bool act = c < C16;
+            float s = 0.0f;
+            uint8_t eb = 0;
+            const uint4 qv = kMx ? mx_quant16_regs(a, b, eb) : fp8_quant16_regs(a, b, s);
+            if (act) {
+#pragma unroll
+                for (int j = 0; j < kQ8RowMaxK; ++j) {
+                    if (j >= k || p[j] < 0)
+                        continue;
+                    st_plain16(recv_q + (size_t)p[j] * H + (size_t)c * 16, qv);
+                    if (kMx) {
+                        if ((c & 1) == 0)
+                            static_cast<uint8_t *>(recv_sc)[(size_t)p[j] * nb + (c >> 1)] = eb;
+                    } else if ((c & 7) == 0) {
+                        static_cast<float *>(recv_sc)[(size_t)p[j] * nb + (c >> 3)] = s;
+                    }
+                }
+            }
+            if (!more)
+                return;
+            t = tn;
+            seg = sn;
+            a = na;
+            b = nb4;
+            if (last_seg)
+                break;
+        }
+    }
+}
+
 // MXFP8 (OCP Microscaling v1.0, E4M3 elements): a 32-column block is two
 // lanes of 16 columns.  Its scale is 2^e, e = floor(log2(amax)) - 8 (the
 // exponent of 448) clamped to [-127, 127] and stored as the E8M0 byte e + 127
@@ -307,19 +388,22 @@ cudaError_t launch_bulk(const uint16_t *x, int T, int H, int k, const int32_t *p
     return cudaGetLastError();
 }
 
-// A persistent grid of (resident CTAs per SM) x (SMs), capped by the work;
-// the occupancy is cached per device.
+// A persistent grid of (resident CTAs per SM) x (SMs), capped at one CTA per
+// warp item (the warps are numbered across CTAs, balanced_warp, so a small
+// batch spreads over as many SMs as it has items); the occupancy is cached
+// per device.
 int persistent_grid(const void *kernel, PerDeviceCache<1> &per_sm_cache, long long warp_items)
 {
     const int per_sm = occupancy_per_sm(per_sm_cache, kernel, kDispThreads, 0);
     const long long g = (long long)device_sm_count() * per_sm;
-    const long long need = (warp_items + kDispThreads / 32 - 1) / (kDispThreads / 32);
-    return (int)(need < g ? need : g);
+    return (int)(warp_items < g ? warp_items : g);
 }
 
 PerDeviceCache<1> g_bf16_per_sm;
 PerDeviceCache<1> g_fp8_per_sm;
 PerDeviceCache<1> g_mx_per_sm;
+PerDeviceCache<1> g_fp8_rows_per_sm;
+PerDeviceCache<1> g_mx_rows_per_sm;
 
 }  // namespace
 
@@ -330,6 +414,11 @@ cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const 
         return cudaSuccess;
     if (use_bulk(T, H, k, 2))
         return launch_bulk<2>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag, st);
+    if (k <= kQ8RowMaxK) {
+        const int grid = persistent_grid((const void *)dispatch_q8_rows_kernel<true>, g_mx_rows_per_sm, T);
+        dispatch_q8_rows_kernel<true><<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
+        return cudaGetLastError();
+    }
     const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_mxfp8_kernel, g_mx_per_sm, items);
     dispatch_mxfp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
@@ -356,6 +445,12 @@ cudaError_t launch_dispatch_fp8(const uint16_t *x, int T, int H, int k, const in
         return cudaSuccess;
     if (use_bulk(T, H, k, 1))
         return launch_bulk<1>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag, st);
+    if (k <= kQ8RowMaxK) {
+        const int grid = persistent_grid((const void *)dispatch_q8_rows_kernel<false>, g_fp8_rows_per_sm, T);
+        dispatch_q8_rows_kernel<false><<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, rows,
+                                                                      err_flag);
+        return cudaGetLastError();
+    }
     const long long items = (long long)T * fp8_segs(H);
     const int grid = persistent_grid((const void *)dispatch_fp8_kernel, g_fp8_per_sm, items);
     dispatch_fp8_kernel<<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_s, rows, err_flag);

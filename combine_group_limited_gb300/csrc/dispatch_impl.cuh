@@ -67,8 +67,14 @@ struct ItemWalk {
     {
         T = T_;
         segs = segs_;
-        const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-        const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+        // Items numbered across CTAs (balanced_warp) when there are few per
+        // warp (small batches: spread over the SMs); CTA by CTA otherwise,
+        // so that a CTA's warps take consecutive segments of the same tokens
+        // (shared pos lines, contiguous rows).
+        const long long nwarps = grid_warps();
+        const long long warp = (long long)T * segs < 2 * nwarps
+                                   ? balanced_warp()
+                                   : (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
         t = warp / segs;
         seg = (int)(warp - t * segs);
         step_t = nwarps / segs;

@@ -74,6 +74,18 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
 }
 
 // 16-byte global load that bypasses L1 allocation (each byte is read once).
+// Warp numbering of the persistent warp kernels: warp w of CTA b is global
+// warp w * gridDim.x + b, so consecutive work units (tokens, row segments)
+// go to different CTAs -- with a grid of whole waves, to different SMs --
+// and every CTA gets the same share of them to within one unit.  (Numbered
+// CTA by CTA, a grid smaller than a full wave left some SMs a CTA more
+// than others, a third more work on Mixtral-sized batches.)
+__device__ __forceinline__ long long balanced_warp()
+{
+    return (long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x;
+}
+__device__ __forceinline__ long long grid_warps() { return ((long long)gridDim.x * blockDim.x) >> 5; }
+
 __device__ __forceinline__ uint4 ld_stream16(const void *p)
 {
     uint4 v;

@@ -52,11 +52,12 @@ def _blocks(B, H, seed):
     return x.reshape(rows, H)
 
 
-@pytest.mark.parametrize("fmt,B,k,rep", [("fp8", 128, 2, 1), ("mxfp8", 32, 2, 1), ("fp8", 128, 4, 13),
-                                          ("mxfp8", 32, 4, 13)])
+@pytest.mark.parametrize("fmt,B,k,rep", [("fp8", 128, 2, 1), ("mxfp8", 32, 2, 1), ("fp8", 128, 5, 1),
+                                          ("mxfp8", 32, 5, 1), ("fp8", 128, 4, 13), ("mxfp8", 32, 4, 13)])
 def test_every_bf16_value_at_every_relative_scale(ep, fmt, B, k, rep):
     """rep > 1 repeats the rows up to a batch the bulk-copy kernel takes
-    (T >= 2048, k >= 4); rep = 1 runs the warp-item kernel."""
+    (T >= 2048, k >= 4); with rep = 1, k <= 4 runs the token-per-warp
+    kernel and k = 5 the warp-item kernel."""
     H = 4096
     x = np.tile(_blocks(B, H, seed=77 + B), (rep, 1))
     T = x.shape[0]
