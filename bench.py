@@ -92,7 +92,7 @@ def measured_hbm_peak():
 
 # The source files each timed kernel is compiled from.
 KERNEL_SOURCES = {
-    "combine_kernel": ("combine.cu", "ep_internal.cuh"),
+    "combine_kernel": ("combine.cu", "coop.cuh", "ep_internal.cuh"),
     "dispatch_bulk_kernel": ("dispatch.cu", "dispatch_impl.cuh", "ep_internal.cuh"),
     "route_kernel": ("route.cu", "coop.cuh", "gate_fast.cuh", "gate_impl.cuh", "ep_internal.cuh"),
 }
