@@ -174,10 +174,7 @@ __device__ __forceinline__ uint4 fp8_quant16_regs(const uint4 &a, const uint4 &b
         nf[2 * i] = bf16_lo(n);
         nf[2 * i + 1] = bf16_hi(n);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        amax = fmaxf(amax, fabsf(nf[i]));
+    float amax = bf16x16_amax(a, b);
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
@@ -298,10 +295,7 @@ __device__ __forceinline__ uint4 mx_quant16_regs(const uint4 &a, const uint4 &b,
         f[2 * i] = bf16_lo(wv[i]);
         f[2 * i + 1] = bf16_hi(wv[i]);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        amax = fmaxf(amax, fabsf(f[i]));
+    float amax = bf16x16_amax(a, b);
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
     // floor(log2(amax)) from the exponent field; zero and fp32 subnormals
     // (below 2^-126) land on the clamp -127.

@@ -47,6 +47,23 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
 // Two fp32 values in one 64-bit register (low, high) for the packed fp32x2
 // arithmetic of sm_100-family GPUs: each lane of a packed op is the IEEE
 // round-to-nearest-even result of the scalar op, so packing changes no bit.
+// The largest magnitude of the 16 bf16 values in a and b, as fp32: a tree
+// of packed max-of-magnitude operations on the bf16 pairs (the sign of each
+// result is not used), then the larger half.  Exact: every candidate is one
+// of the inputs' magnitudes.
+__device__ __forceinline__ float bf16x16_amax(const uint4 &a, const uint4 &b)
+{
+    uint32_t m0, m1, m2, m3;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(a.x), "r"(a.y));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(a.z), "r"(a.w));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(b.x), "r"(b.y));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m3) : "r"(b.z), "r"(b.w));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(m0), "r"(m1));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(m3));
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(m0), "r"(m2));
+    return fmaxf(__uint_as_float((m0 << 16) & 0x7FFF0000u), __uint_as_float(m0 & 0x7FFF0000u));
+}
+
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
 {
     uint64_t r;
