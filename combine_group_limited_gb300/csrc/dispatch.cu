@@ -188,6 +188,115 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_q8_rows_kernel(const ui
     }
 }
 
+// The same walk with kQ8Depth row segments in flight per warp (MXFP8, whose
+// conversion is light enough that the walk waits on its loads; the FP8
+// conversion keeps the issue slots busy and gains nothing): each lane
+// copies its 32 bytes of the next segments into a per-warp ring in shared
+// memory with cp.async (no registers held), waits for the oldest with
+// cp.async.wait_group and reads back only what it copied itself (so no
+// warp barrier is needed).  Mixtral shape: 9.4 -> 8.6 us a call back to
+// back (FP8 with the ring: 10.9 -> 11.5, so FP8 keeps the register walk).
+// Needs fp8_segs(H) >= kQ8Depth, so
+// that the copies in flight span at most the next token, whose pos is then
+// the one prefetched.
+constexpr int kQ8Depth = 4;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool act)
+{
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const int n = act ? 16 : 0;  // src-size 0: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+
+template <bool kMx>
+__global__ void __launch_bounds__(kDispThreads) dispatch_q8_ring_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                                        int k, const int32_t *__restrict__ pos,
+                                                                        uint8_t *__restrict__ recv_q,
+                                                                        void *__restrict__ recv_sc, long long rows,
+                                                                        int32_t *__restrict__ err_flag)
+{
+    __shared__ __align__(16) uint4 ring[kDispThreads / 32][kQ8Depth][32][2];
+    const int lane = threadIdx.x & 31;
+    uint4(*my)[32][2] = ring[threadIdx.x >> 5];
+    const long long nw = grid_warps();
+    const long long t0 = balanced_warp();
+    if (t0 >= T)
+        return;
+    const int segs = fp8_segs(H);
+    const int C16 = H / 16;
+    const int nb = kMx ? H / 32 : H / 128;
+    // producer position (the next segment to copy) and consumer position
+    long long tp = t0, tc = t0;
+    int sp = 0, sc = 0;
+    int pl_next = -1;  // pos of the producer's token when it is ahead of the consumer's
+    auto issue = [&](int slot) {
+        if (tp < T) {
+            const int c = sp * 32 + lane;
+            const bool act = c < C16;
+            const uint16_t *src = x + (size_t)tp * H + (size_t)(act ? c : 0) * 16;
+            cp_async16(&my[slot][lane][0], src, act);
+            cp_async16(&my[slot][lane][1], src + 8, act);
+            if (sp == 0 && tp != tc)
+                pl_next = lane < k ? __ldg(pos + tp * k + lane) : -1;
+            if (++sp == segs) {
+                sp = 0;
+                tp += nw;
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");  // an empty group past the end keeps the count
+    };
+    int pl = lane < k ? __ldg(pos + tc * k + lane) : -1;
+#pragma unroll
+    for (int d = 0; d < kQ8Depth; ++d)
+        issue(d);
+    int p[kQ8RowMaxK];
+    int slot = 0;
+    for (;;) {
+        if (sc == 0) {  // the consumer enters token tc: its checked rows in every lane
+            if (pl >= rows) {
+                if (err_flag)
+                    atomicOr(err_flag, 2);
+                pl = -1;
+            }
+#pragma unroll
+            for (int j = 0; j < kQ8RowMaxK; ++j)
+                p[j] = __shfl_sync(kFullMask, pl, j);
+        }
+        asm volatile("cp.async.wait_group %0;" ::"n"(kQ8Depth - 1) : "memory");
+        const uint4 a = my[slot][lane][0], b = my[slot][lane][1];
+        const int c = sc * 32 + lane;
+        const bool act = c < C16;
+        float s = 0.0f;
+        uint8_t eb = 0;
+        const uint4 qv = kMx ? mx_quant16_regs(a, b, eb) : fp8_quant16_regs(a, b, s);
+        if (act) {
+#pragma unroll
+            for (int j = 0; j < kQ8RowMaxK; ++j) {
+                if (j >= k || p[j] < 0)
+                    continue;
+                st_plain16(recv_q + (size_t)p[j] * H + (size_t)c * 16, qv);
+                if (kMx) {
+                    if ((c & 1) == 0)
+                        static_cast<uint8_t *>(recv_sc)[(size_t)p[j] * nb + (c >> 1)] = eb;
+                } else if ((c & 7) == 0) {
+                    static_cast<float *>(recv_sc)[(size_t)p[j] * nb + (c >> 3)] = s;
+                }
+            }
+        }
+        // the slot is consumed (this lane read its own copies): refill it
+        issue(slot);
+        slot = slot + 1 == kQ8Depth ? 0 : slot + 1;
+        if (++sc == segs) {
+            sc = 0;
+            tc += nw;
+            if (tc >= T)
+                break;
+            pl = pl_next;
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // MXFP8 (OCP Microscaling v1.0, E4M3 elements): a 32-column block is two
 // lanes of 16 columns.  Its scale is 2^e, e = floor(log2(amax)) - 8 (the
 // exponent of 448) clamped to [-127, 127] and stored as the E8M0 byte e + 127
@@ -404,6 +513,7 @@ PerDeviceCache<1> g_fp8_per_sm;
 PerDeviceCache<1> g_mx_per_sm;
 PerDeviceCache<1> g_fp8_rows_per_sm;
 PerDeviceCache<1> g_mx_rows_per_sm;
+PerDeviceCache<1> g_mx_ring_per_sm;
 
 }  // namespace
 
@@ -414,6 +524,11 @@ cudaError_t launch_dispatch_mxfp8(const uint16_t *x, int T, int H, int k, const 
         return cudaSuccess;
     if (use_bulk(T, H, k, 2))
         return launch_bulk<2>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag, st);
+    if (k <= kQ8RowMaxK && fp8_segs(H) >= kQ8Depth) {
+        const int grid = persistent_grid((const void *)dispatch_q8_ring_kernel<true>, g_mx_ring_per_sm, T);
+        dispatch_q8_ring_kernel<true><<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);
+        return cudaGetLastError();
+    }
     if (k <= kQ8RowMaxK) {
         const int grid = persistent_grid((const void *)dispatch_q8_rows_kernel<true>, g_mx_rows_per_sm, T);
         dispatch_q8_rows_kernel<true><<<grid, kDispThreads, 0, st>>>(x, T, H, k, pos, recv_q, recv_e, rows, err_flag);

@@ -75,7 +75,7 @@ def test_dispatch_full_size(ep, name, dtype):
 
 
 @pytest.mark.parametrize("T,H,k", [(1, 8, 1), (3, 24, 2), (17, 128, 3), (33, 384, 8), (9, 7168, 8), (130, 256, 5), (5, 16384, 64),
-                                   (700, 1152, 2), (3000, 640, 1), (301, 384, 4)])
+                                   (700, 1152, 2), (3000, 640, 1), (301, 384, 4), (500, 2176, 3), (2049, 4096, 2)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_dispatch_small_shapes_with_empty_slots(ep, T, H, k, dtype):
     if dtype == "fp8" and H % 128:
@@ -112,14 +112,15 @@ def test_fp8_special_blocks(ep):
     _dispatch_both(ep, x, pos, "bf16")
 
 
-@pytest.mark.parametrize("dtype,k", [("bf16", 4), ("fp8", 4), ("fp8", 6)])
-def test_dispatch_bad_rows_are_flagged_and_skipped(ep, dtype, k):
-    """k = 4: the token-per-warp FP8 kernel; k = 6: the warp-item kernel."""
+@pytest.mark.parametrize("dtype,k,H", [("bf16", 4, 256), ("fp8", 4, 256), ("fp8", 6, 256), ("fp8", 2, 2048)])
+def test_dispatch_bad_rows_are_flagged_and_skipped(ep, dtype, k, H):
+    """FP8 with k <= 4: the token-per-warp kernel; k = 6: the warp-item
+    kernel."""
     rng = np.random.default_rng(8)
-    T, H = 40, 256
+    T = 40
     x = synth.f32_to_bf16_bits(rng.normal(0, 1, (T, H)).astype(np.float32))
     pos = rng.permutation(T * k).reshape(T, k).astype(np.int32)
-    pos[5, 2] = T * k                 # one past the end
+    pos[5, k - 1] = T * k             # one past the end
     pos[17, 0] = 1 << 30
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
     ref_pos = pos.copy()

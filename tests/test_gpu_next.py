@@ -66,6 +66,31 @@ def test_mxfp8_special_blocks(ep):
     np.testing.assert_array_equal(e.cpu().numpy()[rows], re[rows])
 
 
+@pytest.mark.parametrize("T,H,k", [(40, 2048, 2), (301, 2176, 3), (2049, 4096, 1)])
+def test_mxfp8_small_k_rows_in_flight_with_bad_rows(ep, T, H, k):
+    """k <= 4 with at least four row segments per token: the MXFP8 walk that
+    keeps segments in flight through shared memory (a ragged last segment
+    at H = 2176); rows outside the buffer are flagged and skipped, rows no
+    slot names stay untouched."""
+    rng = np.random.default_rng(T + k)
+    x = synth.f32_to_bf16_bits((rng.normal(0, 1, (T, H)) * np.exp2(rng.integers(-8, 8, (T, 1)))).astype(np.float32))
+    pos = rng.permutation(T * k).reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.1] = -1
+    pos[T // 2, k - 1] = T * k + 3
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = torch.full((T * k, H), 0xA5, dtype=torch.uint8, device="cuda")
+    e = torch.full((T * k, H // 32), 0x5A, dtype=torch.uint8, device="cuda")
+    ep.ep_dispatch(dev_bf16(x), dev(pos), "mxfp8", recv=q, recv_scales=e, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 2
+    ref_pos = np.where(pos >= T * k, -1, pos).astype(np.int32)
+    rq = np.full((T * k, H), 0xA5, np.uint8)
+    re = np.full((T * k, H // 32), 0x5A, np.uint8)
+    oracle.dispatch_mxfp8(x, ref_pos, recv_q=rq, recv_e=re)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(e.cpu().numpy(), re)
+
+
 # ------------------------------------------------------- FP8-input combine
 
 
