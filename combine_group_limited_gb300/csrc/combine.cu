@@ -423,11 +423,11 @@ __global__ void __launch_bounds__(kFlatThreads) combine_fp8_flat_kernel(const ui
     st_stream16(dst + 8, o1);
 }
 
-// Batches that take the thread-per-chunk kernels: at most a quarter as many
-// tokens as the CTA kernels have resident CTAs.  Measured on GB300 (H =
-// 7168, k = 8): at 128 tokens they take 3.2 us a call back to back against
-// 5.7 for the CTA kernel; at 512 tokens, 16.0 us against 14.6 (ncu, cold).
-inline bool flat_sized(int T, int cta_per_sm) { return 4LL * T <= (long long)device_sm_count() * cta_per_sm; }
+// Batches that take the thread-per-chunk kernels: at most two tokens per
+// SM.  Measured on GB300 (H = 7168, k = 8): at 128 tokens they take 3.2 us
+// a call back to back against 5.7 for the CTA kernel (FP8 input: 3.5
+// against 4.1); at 512 tokens, 16.0 us against 14.6 (ncu, cold).
+inline bool flat_sized(int T) { return T <= 2 * device_sm_count(); }
 
 // Launches a flat kernel with programmatic stream serialisation.
 template <class... P, class... A>
@@ -644,7 +644,7 @@ cudaError_t launch_combine(const uint16_t *y, long long rows, const int32_t *pos
     }
     static PerDeviceCache<1> occ;  // the same registers either way: sized on the unsplit kernel
     const int per_sm = occupancy_per_sm(occ, (const void *)combine_kernel<false>, kCombThreads, 0);
-    if (flat_sized(T, per_sm))  // decode-sized: one thread per chunk
+    if (flat_sized(T))  // decode-sized: one thread per chunk
         return launch_flat(combine_flat_kernel, (long long)T * (H / 8), st, y, pos, w, T, H, k, out, rows, err_flag);
     const int S = column_segments(T, H / 8, device_sm_count() * per_sm);
     long long grid = (long long)device_sm_count() * per_sm;
@@ -685,7 +685,7 @@ cudaError_t launch_combine_fp8(const uint8_t *yq, const void *yscale, int mx, lo
     const void *kern =
         mx ? (const void *)combine_fp8_kernel<true, false> : (const void *)combine_fp8_kernel<false, false>;
     const int per_sm = occupancy_per_sm(occ, kern, kCombThreads, 0, mx ? 1 : 0);
-    if (flat_sized(T, per_sm)) {  // decode-sized: one thread per chunk
+    if (flat_sized(T)) {  // decode-sized: one thread per chunk
         const long long n = (long long)T * (H / 16);
         return mx ? launch_flat(combine_fp8_flat_kernel<true>, n, st, yq, yscale, pos, w, T, H, k, out, rows, err_flag)
                   : launch_flat(combine_fp8_flat_kernel<false>, n, st, yq, yscale, pos, w, T, H, k, out, rows,
