@@ -494,6 +494,10 @@ cudaError_t launch_route_impl(RouteArgs a, cudaStream_t st)
     int grid, cs;
     route_grid(a.T, grid, cs);
     const int tpc = (a.T + grid - 1) / grid;
+    // a CTA gates all its tokens in one pass of L lanes each: its token count
+    // must fit (tokens past kRtThreads / L would keep unset experts)
+    if (tpc > kRtMaxTok || (kGate && tpc > kRtThreads / L))
+        return cudaErrorInvalidConfiguration;
     const RouteSmem sz = route_smem(tpc, a.k, a.E, a.E / a.epr, L, EPL, a.g.cap, kGate);
     const size_t smem = (sz.gate_words + sz.lay_words) * sizeof(int32_t);
     const void *fn = (const void *)route_kernel<kGate, EPL, L, Q>;
