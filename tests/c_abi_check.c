@@ -3,8 +3,13 @@
  * no PyTorch.  It routes a small DeepSeek-V3-shaped batch (E = 256 experts in
  * 8 groups, top-4 groups, top-8 experts, 32 ranks x 8 experts) with
  * ep_gate_layout, dispatches it (BF16 and FP8), combines identity-expert
- * outputs with the router weights, and checks on the host what the
- * definitions fix:
+ * outputs with the router weights.  Its inputs come from the C generator
+ * (synth/synth.c: the Python tests' DeepSeek-V3 workload, seed 1236, at
+ * T = 512 and H = 256), and it checks the results against the CPU oracle
+ * (oracle/oracle.c, linked as liboracle.so): gating indices, the whole
+ * layout, BF16 rows and FP8 codes and scales bit for bit, weights within
+ * (k+1) binary32 roundings, the combine within max(1 bf16 ulp, 1e-2
+ * relative).  It also checks on the host what the definitions fix:
  *  - every token's experts are distinct, lie in its kept groups and have the
  *    largest keys there (ties to the lower index);
  *  - raw weights sum to one;
@@ -15,7 +20,8 @@
  *    accumulation error (weights sum to one).
  * Exit status 0 on success; the first failed check is printed.
  *
- * Build: cc -I include tests/c_abi_check.c -L <pkg> -lep_gb300 -L <cuda>/lib64 -lcudart -lm
+ * Build: cc -I include -I synth tests/c_abi_check.c synth/synth.c -L <pkg> -lep_gb300
+ *        -L oracle -loracle -L <cuda>/lib64 -lcudart -lm
  */
 #include <cuda_runtime.h>
 #include <math.h>
@@ -25,6 +31,20 @@
 #include <string.h>
 
 #include "ep.h"
+#include "synth.h"
+
+/* The CPU oracle (oracle/oracle.c), test infrastructure only. */
+int orc_gate(const float *scores, const float *bias, int32_t T, int32_t E, int32_t k, int32_t n_groups,
+             int32_t topk_group, int32_t topk_in_group, int32_t score_fn, int32_t normalize, int32_t *topk_idx,
+             double *topk_w);
+int orc_layout(const int32_t *topk_idx, int32_t T, int32_t k, int32_t E, int32_t experts_per_rank,
+               int32_t *expert_count, int32_t *expert_off, int32_t *rank_count, int32_t *rank_off,
+               int32_t *rank_tokens, int32_t *pos, int32_t *src, int32_t *err_flag);
+int orc_dispatch_bf16(const uint16_t *x, int32_t T, int32_t H, int32_t k, const int32_t *pos, uint16_t *recv);
+int orc_dispatch_fp8(const uint16_t *x, int32_t T, int32_t H, int32_t k, const int32_t *pos, uint8_t *recv_q,
+                     float *recv_s);
+int orc_combine(const uint16_t *y, const int32_t *pos, const float *w, int32_t T, int32_t H, int32_t k,
+                uint16_t *out);
 
 #define T 512
 #define H 256
@@ -34,6 +54,8 @@
 #define KG 4
 #define KIN 2
 #define EPR 8
+#define R (E / EPR)
+#define SEED 1236 /* the DeepSeek-V3 workload's seed */
 
 static int fail(const char *what, long a, long b)
 {
@@ -59,18 +81,6 @@ static int fail(const char *what, long a, long b)
         }                                                                            \
     } while (0)
 
-static uint64_t rng_state = 0x243F6A8885A308D3ull;
-
-static uint64_t next_u64(void)
-{
-    uint64_t z = (rng_state += 0x9E3779B97F4A7C15ull);
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
-static float uniform01(void) { return (float)((next_u64() >> 40) + 0.5) / 16777216.0f; }
-
 static float bf16_to_f32(uint16_t b)
 {
     uint32_t u = (uint32_t)b << 16;
@@ -79,26 +89,24 @@ static float bf16_to_f32(uint16_t b)
     return f;
 }
 
-static uint16_t f32_to_bf16(float f)
-{
-    uint32_t u;
-    memcpy(&u, &f, 4);
-    u += 0x7FFFu + ((u >> 16) & 1u); /* round to nearest even (finite inputs) */
-    return (uint16_t)(u >> 16);
-}
 
 int main(void)
 {
     static float scores[T * E], bias[E], w[T * K];
     static uint16_t x[T * H], recv[T * K * H], out[T * H];
-    static int32_t idx[T * K], pos[T * K], src[T * K], ecount[E], eoff[E + 1], rcount[E / EPR], roff[E / EPR + 1],
-        rtok[E / EPR];
-    for (int i = 0; i < T * E; ++i)
-        scores[i] = uniform01();
-    for (int e = 0; e < E; ++e)
-        bias[e] = (uniform01() - 0.5f) * 0.02f;
-    for (int i = 0; i < T * H; ++i)
-        x[i] = f32_to_bf16(uniform01() * 4.0f - 2.0f);
+    static int32_t idx[T * K], pos[T * K], src[T * K], ecount[E], eoff[E + 1], rcount[R], roff[R + 1], rtok[R];
+    static uint8_t q[T * K * H];
+    static float qs[T * K * (H / 128)];
+    /* the DeepSeek-V3 workload's arrays at this T and H: U(0,1) scores,
+     * N(0, 0.01) bias, N(0,1) bf16 rows */
+    synth_uniform_f32(SEED, SYNTH_S_SCORES, (size_t)T * E, scores);
+    {
+        double b64[E];
+        synth_normal_f64(SEED, SYNTH_S_BIAS, E, b64);
+        for (int e = 0; e < E; ++e)
+            bias[e] = (float)(b64[e] * 0.01);
+    }
+    synth_normal_bf16(SEED, SYNTH_S_X, (size_t)T * H, 1.0, x);
 
     const ep_gate_cfg cfg = {E, K, G, KG, KIN, EP_SCORE_RAW, 1};
     size_t wsb = ep_layout_workspace_bytes(T, K, E, EPR);
@@ -150,7 +158,12 @@ int main(void)
     CK(cudaMemcpy(src, d_src, sizeof src, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(ecount, d_ec, sizeof ecount, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(eoff, d_eo, sizeof eoff, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(rcount, d_rc, sizeof rcount, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(roff, d_ro, sizeof roff, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(rtok, d_rt, sizeof rtok, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(recv, d_recv, sizeof recv, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(q, d_q, sizeof q, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(qs, d_sc, sizeof qs, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(out, d_out, sizeof out, cudaMemcpyDeviceToHost));
     if (flag != 0)
         return fail("device error flag", flag, 0);
@@ -233,6 +246,45 @@ int main(void)
             if (fabsf(ov - xv) > tol)
                 return fail("combine of the copies", t, h);
         }
-    printf("c_abi_check ok: %d tokens gated, laid out, dispatched and combined through ep.h\n", T);
+
+    /* parity with the CPU oracle on the same inputs */
+    {
+        static int32_t oidx[T * K], opos[T * K], osrc[T * K], oec[E], oeo[E + 1], orc[R], oro[R + 1], ort[R];
+        static double ow[T * K];
+        static uint16_t orecv[T * K * H], oout[T * H];
+        static uint8_t oq[T * K * H];
+        static float oqs[T * K * (H / 128)];
+        int32_t oflag = 0;
+        if (orc_gate(scores, bias, T, E, K, G, KG, KIN, EP_SCORE_RAW, 1, oidx, ow) != 0)
+            return fail("oracle gate", 0, 0);
+        for (int i = 0; i < T * K; ++i) {
+            if (idx[i] != oidx[i])
+                return fail("gate index vs oracle", i, oidx[i]);
+            if (fabs((double)w[i] - ow[i]) > (K + 1) * 5.96e-8 * fabs(ow[i]))
+                return fail("gate weight vs oracle", i, 0);
+        }
+        if (orc_layout(oidx, T, K, E, EPR, oec, oeo, orc, oro, ort, opos, osrc, &oflag) != 0 || oflag != 0)
+            return fail("oracle layout", oflag, 0);
+        if (memcmp(ecount, oec, sizeof oec) || memcmp(eoff, oeo, sizeof oeo) || memcmp(rcount, orc, sizeof orc) ||
+            memcmp(roff, oro, sizeof oro) || memcmp(rtok, ort, sizeof ort) || memcmp(pos, opos, sizeof opos) ||
+            memcmp(src, osrc, sizeof osrc))
+            return fail("layout vs oracle", 0, 0);
+        memset(orecv, 0, sizeof orecv);
+        if (orc_dispatch_bf16(x, T, H, K, opos, orecv) != 0 || memcmp(recv, orecv, sizeof orecv))
+            return fail("bf16 dispatch vs oracle", 0, 0);
+        if (orc_dispatch_fp8(x, T, H, K, opos, oq, oqs) != 0 || memcmp(q, oq, sizeof oq) || memcmp(qs, oqs, sizeof oqs))
+            return fail("fp8 dispatch vs oracle", 0, 0);
+        if (orc_combine(orecv, opos, w, T, H, K, oout) != 0)
+            return fail("oracle combine", 0, 0);
+        for (int i = 0; i < T * H; ++i) {
+            const float g = bf16_to_f32(out[i]), r = bf16_to_f32(oout[i]);
+            const float ulp = fabsf(r) * (1.0f / 128.0f); /* one bf16 ulp is at most 2^-7 |r| */
+            const float bar = fmaxf(ulp, 1e-2f * fabsf(r));
+            if (fabsf(g - r) > bar + 1e-30f)
+                return fail("combine vs oracle", i / H, i % H);
+        }
+    }
+    printf("c_abi_check ok: %d tokens gated, laid out, dispatched and combined through ep.h; "
+           "matches the oracle\n", T);
     return 0;
 }
