@@ -546,9 +546,12 @@ def run_ours(args):
             "e2e": {"value": round(rep.tokens_per_s(T, e2e["ms"]), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "ms_per_step": round(e2e["ms"], 4),
-                    "method": "public API, pinned host buffers; H2D of scores then x in %d token chunks, "
-                              "dispatch+combine per chunk, D2H per chunk, on three streams%s"
-                              % (e2e["chunks"], ", the step's calls captured once as a CUDA graph and replayed"
+                    "method": "public API, pinned host buffers; per step H2D of scores then x in %d token "
+                              "chunks, dispatch+combine per chunk, D2H per chunk, on three streams, two device "
+                              "buffer sets so that a step's uploads overlap the previous step; %d consecutive "
+                              "steps timed together%s; the last step's output checked against the "
+                              "device-resident path"
+                              % (e2e["chunks"], e2e["steps"], ", captured once as a CUDA graph and replayed"
                                  if e2e["graph"] else "")},
             "cpu_baseline": cpu,
             "configs": configs,
@@ -559,88 +562,128 @@ def run_ours(args):
     rep.close()
 
 
-def run_e2e(r, args, chunks=8, graph=True):
-    """The same path through the public API with host buffers: the step's
-    inputs are copied in from pinned host memory and its output copied back,
-    inside the timed region.  The copies overlap the kernels the way a caller
-    of this API would arrange it: the scores go first so that gating and
-    layout run while the hidden rows stream in by token chunks; each chunk is
-    dispatched and combined as soon as it has landed and its output rows are
-    copied back on a third stream."""
+def run_e2e(r, args, chunks=16, graph=True, steps=10):
+    """The same path through the public API with host buffers: every step's
+    inputs (scores, bias, hidden rows) are copied in from pinned host memory
+    and its output copied back, inside the timed region.  The copies overlap
+    the kernels the way a caller streaming batches through this API would
+    arrange it, on three streams:
+      - the scores go first, so that gating and layout run while the hidden
+        rows stream in by token chunks; each chunk is dispatched and combined
+        as soon as it has landed, and its output rows go back on a third
+        stream;
+      - two sets of device buffers alternate between steps, so step i+1's
+        uploads run while step i computes and downloads (a set is refilled
+        once the step two back has read its inputs and downloaded its
+        output).
+    The kernels run in order on one stream.  `steps` consecutive steps are
+    timed together (one CUDA graph when `graph`); the result is per step,
+    and the last step's downloaded output is checked against the same path
+    run on device-resident inputs."""
     import torch
     ep = r.ep
     c = r.cfg
-    T, H, k = c["T"], c["H"], c["k"]
+    T, H, k, E, epr = c["T"], c["H"], c["k"], c["E"], c["experts_per_rank"]
     hs = torch.from_numpy(r.host["scores"]).pin_memory()
     hb = None if r.host["bias"] is None else torch.from_numpy(r.host["bias"]).pin_memory()
     hx = torch.from_numpy(r.host["x"].view(np.int16)).pin_memory()
     ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
+    sets = []
+    for p in range(2):
+        sets.append(dict(
+            scores=torch.empty_like(r.scores), bias=None if r.bias is None else torch.empty_like(r.bias),
+            x=torch.empty_like(r.x), idx=torch.empty_like(r.topk_idx), w=torch.empty_like(r.topk_w),
+            lay=ep.alloc_layout(T, k, E, epr, r.x.device), out=torch.empty_like(r.out)))
     comp = torch.cuda.Stream()  # a side stream: graphs are captured off the default stream
     comp.wait_stream(torch.cuda.current_stream())
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     bounds = [T * i // chunks for i in range(chunks + 1)]
-    xi = r.x.view(torch.int16)
-    oi = r.out.view(torch.int16)
-    n = max(1, min(args.steps, 10))
 
-    def one():
+    def run_steps():
         s_in.wait_stream(comp)
-        with torch.cuda.stream(s_in):
-            r.scores.copy_(hs, non_blocking=True)
-            if hb is not None:
-                r.bias.copy_(hb, non_blocking=True)
-            ev_scores = torch.cuda.Event()
-            ev_scores.record(s_in)
-            ev_x = []
-            for i in range(chunks):
-                a, b = bounds[i], bounds[i + 1]
-                xi[a:b].copy_(hx[a:b], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(s_in)
-                ev_x.append(ev)
-        comp.wait_event(ev_scores)
-        r.route()
-        for i in range(chunks):
-            a, b = bounds[i], bounds[i + 1]
-            comp.wait_event(ev_x[i])
-            ep.ep_dispatch(r.x[a:b], r.lay.pos[a:b], "fp8", recv=r.recv_q, recv_scales=r.recv_s, err_flag=r.err)
-            ep.ep_combine(r.y, r.lay.pos[a:b], r.topk_w[a:b], out=r.out[a:b], err_flag=r.err)
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            s_out.wait_event(ev)
-            with torch.cuda.stream(s_out):
-                ho[a:b].copy_(oi[a:b], non_blocking=True)
+        s_out.wait_stream(comp)
+        done = []  # (compute done, download done) events per step
+        for i in range(steps):
+            S = sets[i % 2]
+            xi, oi = S["x"].view(torch.int16), S["out"].view(torch.int16)
+            if i >= 2:
+                s_in.wait_event(done[i - 2][0])     # the set's inputs were read
+            with torch.cuda.stream(s_in):
+                S["scores"].copy_(hs, non_blocking=True)
+                if hb is not None:
+                    S["bias"].copy_(hb, non_blocking=True)
+                ev_scores = torch.cuda.Event()
+                ev_scores.record(s_in)
+                ev_x = []
+                for ci in range(chunks):
+                    a, b = bounds[ci], bounds[ci + 1]
+                    xi[a:b].copy_(hx[a:b], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_in)
+                    ev_x.append(ev)
+            comp.wait_event(ev_scores)
+            if i >= 2:
+                comp.wait_event(done[i - 2][1])    # the set's output was downloaded
+            with torch.cuda.stream(comp):
+                ep.ep_gate_layout(S["scores"], S["bias"], r.gcfg, epr, topk_idx=S["idx"], topk_w=S["w"],
+                                  out=S["lay"], workspace=r.ws, err_flag=r.err)
+                for ci in range(chunks):
+                    a, b = bounds[ci], bounds[ci + 1]
+                    comp.wait_event(ev_x[ci])
+                    ep.ep_dispatch(S["x"][a:b], S["lay"].pos[a:b], "fp8", recv=r.recv_q, recv_scales=r.recv_s,
+                                   err_flag=r.err)
+                    ep.ep_combine(r.y, S["lay"].pos[a:b], S["w"][a:b], out=S["out"][a:b], err_flag=r.err)
+                    ev = torch.cuda.Event()
+                    ev.record(comp)
+                    s_out.wait_event(ev)
+                    with torch.cuda.stream(s_out):
+                        ho[a:b].copy_(oi[a:b], non_blocking=True)
+                ev_c = torch.cuda.Event()
+                ev_c.record(comp)
+            ev_o = torch.cuda.Event()
+            ev_o.record(s_out)
+            done.append((ev_c, ev_o))
+        comp.wait_stream(s_in)
         comp.wait_stream(s_out)
 
     with torch.cuda.stream(comp):
-        return _time_e2e(one, comp, n, graph, hs, hb, hx, ho, chunks)
-
-
-def _time_e2e(one, comp, n, graph, hs, hb, hx, ho, chunks):
-    import torch
-    for _ in range(2):
-        one()
+        res = _time_e2e(run_steps, comp, steps, graph, hs, hb, hx, ho, chunks)
+    # the downloaded output equals the same path on device-resident inputs
+    r.route()
+    r.dispatch()
+    r.combine()
     torch.cuda.synchronize()
-    run = one
+    if not torch.equal(ho, r.out.view(torch.int16).cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident path")
+    return res
+
+
+def _time_e2e(run_steps, comp, steps, graph, hs, hb, hx, ho, chunks):
+    import torch
+    run_steps()
+    torch.cuda.synchronize()
+    run = run_steps
     if graph:
-        # The step's calls (copies, the C-ABI launches, the stream joins)
+        # The steps' calls (copies, the C-ABI launches, the stream joins)
         # recorded once as a CUDA graph and replayed: per-chunk host work
         # (Python, argument checks, launch calls) then stays off the timed
-        # path, as in a caller that captures its steady-state step.
+        # path, as in a caller that captures its steady-state loop.
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=comp):
-            one()
+            run_steps()
         g.replay()
         torch.cuda.synchronize()
         run = g.replay
+    reps = 3
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
-    for _ in range(n):
+    for _ in range(reps):
         run()
     b.record(comp)
     b.synchronize()
     h2d = hs.numel() * 4 + (0 if hb is None else hb.numel() * 4) + hx.numel() * 2
-    return {"ms": a.elapsed_time(b) / n, "h2d": h2d, "d2h": ho.numel() * 2, "chunks": chunks, "graph": graph}
+    return {"ms": a.elapsed_time(b) / (reps * steps), "h2d": h2d, "d2h": ho.numel() * 2, "chunks": chunks,
+            "graph": graph, "steps": steps}
 
 
 def _oracle_path(cfg, inp, y_bits):
@@ -869,7 +912,10 @@ def main():
     ap.add_argument("--configs", default="", help="comma-separated workloads for --sweep")
     ap.add_argument("--ops", default="", help="comma-separated ops for --sweep (default: all)")
     ap.add_argument("--no-hot", action="store_true", help="--sweep: skip the graph-replayed back-to-back timing")
-    ap.add_argument("--e2e-chunks", type=int, default=16,
+    # 4 chunks of 2048 tokens: with the next step's uploads overlapping, fewer
+    # and larger copies use the host link best (GB300: 16 chunks 0.88 ms a
+    # step, 8 0.82, 4 0.80, 2 0.80)
+    ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="token chunks the end-to-end leg pipelines its copies and kernels over")
     ap.add_argument("--e2e-no-graph", action="store_true",
                     help="issue the end-to-end leg's calls from Python every step instead of replaying a CUDA graph")
