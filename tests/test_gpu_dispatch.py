@@ -75,7 +75,8 @@ def test_dispatch_full_size(ep, name, dtype):
 
 
 @pytest.mark.parametrize("T,H,k", [(1, 8, 1), (3, 24, 2), (17, 128, 3), (33, 384, 8), (9, 7168, 8), (130, 256, 5), (5, 16384, 64),
-                                   (700, 1152, 2), (3000, 640, 1), (301, 384, 4), (500, 2176, 3), (2049, 4096, 2)])
+                                   (700, 1152, 2), (3000, 640, 1), (301, 384, 4), (500, 2176, 3), (2049, 4096, 2),
+                                   (128, 7168, 2), (1000, 4608, 4)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_dispatch_small_shapes_with_empty_slots(ep, T, H, k, dtype):
     if dtype == "fp8" and H % 128:

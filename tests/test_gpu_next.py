@@ -66,11 +66,12 @@ def test_mxfp8_special_blocks(ep):
     np.testing.assert_array_equal(e.cpu().numpy()[rows], re[rows])
 
 
-@pytest.mark.parametrize("T,H,k", [(40, 2048, 2), (301, 2176, 3), (2049, 4096, 1)])
+@pytest.mark.parametrize("T,H,k", [(40, 2048, 2), (301, 2176, 3), (2049, 4096, 1), (128, 7168, 2), (1000, 4608, 4)])
 def test_mxfp8_small_k_rows_in_flight_with_bad_rows(ep, T, H, k):
     """k <= 4 with at least four row segments per token: the MXFP8 walk that
     keeps segments in flight through shared memory (a ragged last segment
-    at H = 2176); rows outside the buffer are flagged and skipped, rows no
+    at H = 2176; tokens split into pieces of 4 and 5 segments at H = 7168
+    and 4608); rows outside the buffer are flagged and skipped, rows no
     slot names stay untouched."""
     rng = np.random.default_rng(T + k)
     x = synth.f32_to_bf16_bits((rng.normal(0, 1, (T, H)) * np.exp2(rng.integers(-8, 8, (T, 1)))).astype(np.float32))
@@ -142,6 +143,9 @@ def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     ("fp8", 2048, 1024, 6, 4),
     # k <= 2 on large batches: one warp per token
     ("fp8", 2048, 1024, 2, 0), ("mxfp8", 2100, 96, 1, 0), ("fp8", 2500, 384, 2, 4),
+    # k <= 2 with rows of several rounds of chunks per lane (the next round's
+    # codes copied ahead), the last one ragged
+    ("fp8", 600, 4224, 2, 4), ("mxfp8", 333, 7168, 1, 0), ("mxfp8", 700, 2560, 2, 0),
 ])
 def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset):
     rng = np.random.default_rng(9 + T + H)
