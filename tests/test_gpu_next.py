@@ -168,6 +168,32 @@ def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset)
     _assert_fp8_combine_close(host_bits(out), r, _dequant(q, s, 128 if fmt == "fp8" else 32), pos, w)
 
 
+@pytest.mark.parametrize("fmt,H,k", [("fp8", 2176, 3), ("mxfp8", 2048, 8), ("fp8", 7168, 3), ("mxfp8", 2176, 5)])
+def test_combine_fp8_large_batch_ragged_rows_with_bad_rows(ep, fmt, H, k):
+    """2 < k <= 8 on 2048+ tokens, the CTA kernel: rows of 136, 128 and 448
+    chunks of 16 codes (one pass and a partial second pass of the CTA's
+    threads at 136 and 448); a row outside the buffer is flagged and
+    skipped, empty slots add nothing."""
+    rng = np.random.default_rng(H + k)
+    T = 2100
+    rows = T * k
+    q = rng.integers(0, 256, size=(rows, H)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3C
+    s = (rng.uniform(0.01, 3, (rows, H // 128)).astype(np.float32) if fmt == "fp8"
+         else rng.integers(110, 140, (rows, H // 32)).astype(np.uint8))
+    pos = rng.permutation(rows).reshape(T, k).astype(np.int32)
+    pos[rng.random((T, k)) < 0.15] = -1
+    pos[T // 3, k - 1] = rows + 7
+    w = rng.uniform(-1, 1, (T, k)).astype(np.float32)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = ep.ep_combine_fp8(dev(q), dev(s), dev(pos), dev(w), err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 2
+    ref_pos = np.where(pos >= rows, -1, pos).astype(np.int32)
+    r = oracle.combine_fp8(q, s, ref_pos, w)
+    _assert_fp8_combine_close(host_bits(out), r, _dequant(q, s, 128 if fmt == "fp8" else 32), ref_pos, w)
+
+
 @pytest.mark.parametrize("fmt", ["fp8", "mxfp8"])
 def test_combine_fp8_decode_sized_batch_equals_rows_of_a_large_batch(ep, fmt):
     """Fewer tokens than resident CTAs: the thread-per-chunk kernel; its rows
