@@ -64,6 +64,8 @@ uint16_t synth_f32_to_bf16(float f)
 
 void synth_normal_bf16(uint64_t seed, uint64_t stream, size_t n, double sigma, uint16_t *out)
 {
+    if (n == 0)
+        return;
     double *z = malloc(n * sizeof(double));
     if (!z)
         abort();
