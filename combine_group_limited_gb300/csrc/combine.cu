@@ -208,8 +208,16 @@ __device__ __forceinline__ void pack_acc16(const uint64_t (&acc)[8], uint4 &o0, 
 }
 
 // kMx: scales are E8M0 bytes per 32 columns; else fp32 per 128 columns.
+// Slots are summed kFp8SlotBatch at a time (all loads of a batch issued
+// before its conversions), and the kernel is held to five CTAs per SM: the
+// decode arithmetic per byte is about twice the BF16 combine's, and more
+// resident warps overlap it with the loads better than more loads in flight
+// per thread.  DSV3 shape (ncu, L2 flushed): 96.3 us against 102.7 us with
+// batches of 8 slots at three CTAs per SM, 98.5 us at four CTAs per SM.
+constexpr int kFp8SlotBatch = 4;
+
 template <bool kMx, bool kSplit>
-__global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t *__restrict__ yq,
+__global__ void __launch_bounds__(kCombThreads, 5) combine_fp8_kernel(const uint8_t *__restrict__ yq,
                                                                    const void *__restrict__ yscale,
                                                                    const int32_t *__restrict__ pos,
                                                                    const float *__restrict__ w, int T, int H, int k,
@@ -258,13 +266,13 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
             for (int i = 0; i < 8; ++i)
                 acc[i] = 0ull;
             const int sb = kMx ? (c >> 1) : (c >> 3);  // this lane's scale block
-            for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+            for (int j0 = 0; j0 < k; j0 += kFp8SlotBatch) {
                 // First issue every load of the batch (codes and raw scale
                 // words), then convert: no load waits behind a conversion.
-                uint4 v[kSlotBatch];
-                uint32_t sraw[kSlotBatch];
+                uint4 v[kFp8SlotBatch];
+                uint32_t sraw[kFp8SlotBatch];
 #pragma unroll
-                for (int u = 0; u < kSlotBatch; ++u) {
+                for (int u = 0; u < kFp8SlotBatch; ++u) {
                     const int j = j0 + u;
                     const int p = j < k ? s_pos[j] : -1;
                     if (p >= 0) {
@@ -274,7 +282,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_fp8_kernel(const uint8_t
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < kSlotBatch; ++u) {
+                for (int u = 0; u < kFp8SlotBatch; ++u) {
                     const int j = j0 + u;
                     const int p = j < k ? s_pos[j] : -1;
                     if (p >= 0) {
