@@ -146,6 +146,9 @@ def test_combine_fp8_full_size_identity_experts(ep, name, fmt):
     # k <= 2 with rows of several rounds of chunks per lane (the next round's
     # codes copied ahead), the last one ragged
     ("fp8", 600, 4224, 2, 4), ("mxfp8", 333, 7168, 1, 0), ("mxfp8", 700, 2560, 2, 0),
+    # fewer tokens than resident CTAs but more than the thread-per-chunk
+    # kernel takes: the CTA kernel with each row split over two CTAs
+    ("fp8", 500, 4096, 6, 4), ("mxfp8", 400, 7168, 8, 0),
 ])
 def test_combine_fp8_random_codes_signed_weights(ep, fmt, T, H, k, scale_offset):
     rng = np.random.default_rng(9 + T + H)
