@@ -317,9 +317,16 @@ __device__ __forceinline__ int dc_row(const int32_t *s_e, const int32_t *s_pre, 
     return s_off[e] + s_pre[e] + __popcll(s_mask[e] & ((1ull << j) - 1ull));
 }
 
-template <int EPL>
+// kDt: the payload the body is compiled for: -1 none (gating and layout
+// only), 1 FP8 1x128 (the decode path's usual payload), kDtAny the others
+// (BF16, MXFP8), taken from a.dtype at run time.  A body specialised to FP8
+// measured 7.28 against 7.48 us a call back to back (decode shape).
+constexpr int kDtAny = 3;
+
+template <int EPL, int kDt>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const DecodeArgs a)
 {
+    const int dtype = kDt == kDtAny ? a.dtype : kDt;
     extern __shared__ __align__(16) unsigned char dc_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.gp.E, k = a.gp.k, T = a.T, R = E / a.epr;
@@ -349,13 +356,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const De
     // this CTA's warp items (token, row segment); this cluster's share is
     // items i0, i0 + G * warps, ... for each warp, whose first row segment
     // is loaded now
-    const int segs = a.dtype < 0 ? 0 : a.dtype == 0 ? bf16_segs(a.H) : fp8_segs(a.H);
+    const int segs = dtype < 0 ? 0 : dtype == 0 ? bf16_segs(a.H) : fp8_segs(a.H);
     const int n_items = n_loc * segs;
     const int i0 = cid + G * warp;
     uint4 v[kBf16Unroll];
     if (i0 < n_items) {
         const int t = t_lo + i0 / segs, seg = i0 % segs;
-        if (a.dtype == 0)
+        if (dtype == 0)
             bf16_item_load(a.x, a.H, t, seg, v);
         else
             q8_item_load(a.x, a.H, t, seg, v[0], v[1]);
@@ -393,9 +400,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const De
     uint4 qv = v[0];
     float qs = 0.0f;
     uint8_t qe = 0;
-    if (i0 < n_items && a.dtype == 1)
+    if (i0 < n_items && dtype == 1)
         qv = fp8_quant16_regs(v[0], v[1], qs);
-    else if (i0 < n_items && a.dtype == 2)
+    else if (i0 < n_items && dtype == 2)
         qv = mx_quant16_regs(v[0], v[1], qe);
     cluster_wait();  // every CTA's counts are here; no remote access follows
 
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const De
         const int t = t_lo + j;
         const bool first = item == i0;  // its row segment is loaded (and converted) already
         if (!first) {
-            if (a.dtype == 0)
+            if (dtype == 0)
                 bf16_item_load(a.x, a.H, t, seg, v);
             else
                 q8_item_load(a.x, a.H, t, seg, v[0], v[1]);
@@ -484,12 +491,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_cluster_kernel(const De
                 atomicOr(a.err_flag, 2);
             p0 = -1;
         }
-        if (a.dtype == 0)
+        if (dtype == 0)
             bf16_item_store(a.H, k, seg, p0, -1, v, static_cast<uint16_t *>(a.recv));
-        else if (a.dtype == 1 && first)
+        else if (dtype == 1 && first)
             fp8_item_put(a.H, k, seg, p0, -1, qv, qs, static_cast<uint8_t *>(a.recv),
                          static_cast<float *>(a.recv_scales));
-        else if (a.dtype == 1)
+        else if (dtype == 1)
             fp8_item_store(a.H, k, seg, p0, -1, v[0], v[1], static_cast<uint8_t *>(a.recv),
                            static_cast<float *>(a.recv_scales));
         else if (first)
@@ -550,9 +557,14 @@ cudaError_t launch_cluster_epl(DecodeArgs a, cudaStream_t st)
 {
     int warp_floats;
     gate_plan<EPL>(a.gp, a.scores, a.bias, a.group_lanes, a.vec_rows, warp_floats);
-    const void *fn = (const void *)decode_cluster_kernel<EPL>;
-    static PerDeviceCache<1> smem_attr;
-    const cudaError_t e = raise_smem_limit(smem_attr, fn, kDcMaxSmem);
+    // the body for this payload, and its per-device launch caches
+    const int var = a.dtype < 0 ? 0 : a.dtype == 1 ? 1 : 2;
+    void (*const kern)(DecodeArgs) = var == 0   ? decode_cluster_kernel<EPL, -1>
+                                     : var == 1 ? decode_cluster_kernel<EPL, 1>
+                                                : decode_cluster_kernel<EPL, kDtAny>;
+    const void *fn = (const void *)kern;
+    static PerDeviceCache<1> smem_attr[3];
+    const cudaError_t e = raise_smem_limit(smem_attr[var], fn, kDcMaxSmem);
     if (e != cudaSuccess)
         return e;
     const int cs = a.T < kDcMaxCluster ? a.T : kDcMaxCluster;
@@ -574,8 +586,8 @@ cudaError_t launch_cluster_epl(DecodeArgs a, cudaStream_t st)
     if (a.dtype >= 0) {
         const int segs = a.dtype == 0 ? bf16_segs(a.H) : fp8_segs(a.H);
         G = tpc * segs;
-        static PerDeviceCache<kDcMaxCluster + 1> resident;
-        const int most = resident.get(
+        static PerDeviceCache<kDcMaxCluster + 1> resident[3];
+        const int most = resident[var].get(
             [&] {
                 cudaLaunchConfig_t q = {};
                 q.gridDim = dim3((unsigned)cs);
@@ -602,7 +614,7 @@ cudaError_t launch_cluster_epl(DecodeArgs a, cudaStream_t st)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<EPL>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // The clustered kernel when the batch fits its token masks, else (or if the
