@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) route_kernel(const RouteArgs a)
     const int ncl = C / (int)cs, cl = cta / (int)cs;
     const int tpc = (T + C - 1) / C;  // the most tokens a CTA holds (shared-memory sizing)
     const int nb = (ntok + kBlk - 1) / kBlk, NB = (tpc + kBlk - 1) / kBlk;
-    const bool capped = a.cap >= 0;
+    const bool capped = !kGate && a.cap >= 0;  // routing with gating is always dropless
     const RouteSmem sz = route_smem(tpc, k, E, R, L, EPL, a.g.cap, kGate);
     int32_t *s_row = rsm + sz.gate_words;  // [E4] this CTA's entries per expert (read by the cluster)
     int32_t *s_pre = s_row + E4;           // [E4] entries of lower CTAs
@@ -189,7 +189,12 @@ __global__ void __launch_bounds__(kRtThreads, 1) route_kernel(const RouteArgs a)
         atomicOr(s_mask + (size_t)blk * E + e, bit);
         atomicOr(s_rmask + (size_t)blk * R + e / epr, bit);
     }
-    const bool any_dup = __syncthreads_or(dup) != 0;
+    // gating chooses distinct experts per token: no repeats to count
+    bool any_dup = false;
+    if (kGate)
+        __syncthreads();
+    else
+        any_dup = __syncthreads_or(dup) != 0;
     if (any_dup) {
         // an expert repeated within a token: count the entries one by one
         for (int i = tid; i < NB * E; i += kRtThreads)
