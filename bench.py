@@ -508,7 +508,7 @@ def run_ours(args):
     ms_per_step = rep.max(sum(step_ms) / args.steps)
 
     # end to end through the public API: pinned host inputs -> device -> path -> host output
-    e2e = run_e2e(r, args, chunks=args.e2e_chunks, graph=not args.e2e_no_graph)
+    e2e = run_e2e(r, args, chunks=args.e2e_chunks, graph=not args.e2e_no_graph, nsets=args.e2e_sets)
     e2e["ms"] = rep.max(e2e["ms"])
 
     configs = None
@@ -564,12 +564,12 @@ def run_ours(args):
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "ms_per_step": round(e2e["ms"], 4),
                     "method": "public API, pinned host buffers; per step H2D of scores then x in %d token "
-                              "chunks, dispatch+combine per chunk, D2H per chunk, on three streams, two device "
+                              "chunks, dispatch+combine per chunk, D2H per chunk, on three streams, %d device "
                               "buffer sets so that a step's uploads overlap the previous step; %d consecutive "
                               "steps timed together%s; the last step's output checked against the "
                               "device-resident path"
-                              % (e2e["chunks"], e2e["steps"], ", captured once as a CUDA graph and replayed"
-                                 if e2e["graph"] else "")},
+                              % (e2e["chunks"], e2e["sets"], e2e["steps"],
+                                 ", captured once as a CUDA graph and replayed" if e2e["graph"] else "")},
             "cpu_baseline": cpu,
             "configs": configs,
             "clocks": clk.summary(),
@@ -579,7 +579,7 @@ def run_ours(args):
     rep.close()
 
 
-def run_e2e(r, args, chunks=16, graph=True, steps=10):
+def run_e2e(r, args, chunks=16, graph=True, steps=10, nsets=2):
     """The same path through the public API with host buffers: every step's
     inputs (scores, bias, hidden rows) are copied in from pinned host memory
     and its output copied back, inside the timed region.  The copies overlap
@@ -589,9 +589,9 @@ def run_e2e(r, args, chunks=16, graph=True, steps=10):
         rows stream in by token chunks; each chunk is dispatched and combined
         as soon as it has landed, and its output rows go back on a third
         stream;
-      - two sets of device buffers alternate between steps, so step i+1's
+      - `nsets` sets of device buffers rotate between steps, so step i+1's
         uploads run while step i computes and downloads (a set is refilled
-        once the step two back has read its inputs and downloaded its
+        once the step nsets back has read its inputs and downloaded its
         output).
     The kernels run in order on one stream.  `steps` consecutive steps are
     timed together (one CUDA graph when `graph`); the result is per step,
@@ -606,7 +606,7 @@ def run_e2e(r, args, chunks=16, graph=True, steps=10):
     hx = torch.from_numpy(r.host["x"].view(np.int16)).pin_memory()
     ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
     sets = []
-    for p in range(2):
+    for p in range(nsets):
         sets.append(dict(
             scores=torch.empty_like(r.scores), bias=None if r.bias is None else torch.empty_like(r.bias),
             x=torch.empty_like(r.x), idx=torch.empty_like(r.topk_idx), w=torch.empty_like(r.topk_w),
@@ -621,10 +621,10 @@ def run_e2e(r, args, chunks=16, graph=True, steps=10):
         s_out.wait_stream(comp)
         done = []  # (compute done, download done) events per step
         for i in range(steps):
-            S = sets[i % 2]
+            S = sets[i % nsets]
             xi, oi = S["x"].view(torch.int16), S["out"].view(torch.int16)
-            if i >= 2:
-                s_in.wait_event(done[i - 2][0])     # the set's inputs were read
+            if i >= nsets:
+                s_in.wait_event(done[i - nsets][0])     # the set's inputs were read
             with torch.cuda.stream(s_in):
                 S["scores"].copy_(hs, non_blocking=True)
                 if hb is not None:
@@ -639,8 +639,8 @@ def run_e2e(r, args, chunks=16, graph=True, steps=10):
                     ev.record(s_in)
                     ev_x.append(ev)
             comp.wait_event(ev_scores)
-            if i >= 2:
-                comp.wait_event(done[i - 2][1])    # the set's output was downloaded
+            if i >= nsets:
+                comp.wait_event(done[i - nsets][1])    # the set's output was downloaded
             with torch.cuda.stream(comp):
                 ep.ep_gate_layout(S["scores"], S["bias"], r.gcfg, epr, topk_idx=S["idx"], topk_w=S["w"],
                                   out=S["lay"], workspace=r.ws, err_flag=r.err)
@@ -665,6 +665,7 @@ def run_e2e(r, args, chunks=16, graph=True, steps=10):
 
     with torch.cuda.stream(comp):
         res = _time_e2e(run_steps, comp, steps, graph, hs, hb, hx, ho, chunks)
+    res["sets"] = nsets
     # the downloaded output equals the same path on device-resident inputs
     r.route()
     r.dispatch()
@@ -934,6 +935,8 @@ def main():
     # step, 8 0.82, 4 0.80, 2 0.80)
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="token chunks the end-to-end leg pipelines its copies and kernels over")
+    ap.add_argument("--e2e-sets", type=int, default=2,
+                    help="device buffer sets the end-to-end leg rotates between steps")
     ap.add_argument("--e2e-no-graph", action="store_true",
                     help="issue the end-to-end leg's calls from Python every step instead of replaying a CUDA graph")
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per op in --sweep")
