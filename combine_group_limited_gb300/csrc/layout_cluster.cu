@@ -65,6 +65,9 @@ __host__ __device__ inline size_t lc_smem_words(int nb, int E, int R, int k)
     return (size_t)nb * (2 * E + R) + 3 * (size_t)E + R + (size_t)nb * kBlk * k;
 }
 
+// kCap: capacity mode (a.cap >= 0); the dropless instance is compiled
+// without the capacity paths (a smaller body to fetch on a cold call).
+template <bool kCap>
 __global__ void __launch_bounds__(kLcThreads, 1) layout_cluster_kernel(const LcArgs a)
 {
     extern __shared__ __align__(16) int32_t lsm[];
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kLcThreads, 1) layout_cluster_kernel(const LcA
     __shared__ int32_t s_total;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, k = a.k, E = a.E, epr = a.epr, R = E / epr, NB = a.nb;
-    const bool capped = a.cap >= 0;
+    const bool capped = kCap;
     const unsigned C = cluster_nctarank(), c = cluster_ctarank();
     const int B = (T + kBlk - 1) / kBlk;
     const int b0 = (int)((long long)B * c / C), b1 = (int)((long long)B * (c + 1) / C);
@@ -310,21 +313,20 @@ __global__ void __launch_bounds__(kLcThreads, 1) layout_cluster_kernel(const LcA
 
 // The cluster size this device runs the kernel at: 16 CTAs of one SM each
 // where the device allows non-portable cluster sizes and can co-schedule
-// them, else 8; 0 if neither fits.
-int cluster_size_for(size_t smem)
+// them, else 8; 0 if neither fits.  One answer for both instances (the
+// smaller of the two), so that the support check and the launch agree.
+template <bool kCap>
+int cluster_size_of()
 {
+    const void *fn = (const void *)layout_cluster_kernel<kCap>;
     static PerDeviceCache<1> attr;
-    const cudaError_t ae = raise_smem_limit(attr, (const void *)layout_cluster_kernel, kLcMaxSmem);
+    const cudaError_t ae = raise_smem_limit(attr, fn, kLcMaxSmem);
     if (ae != cudaSuccess)
         return 0;
     static PerDeviceCache<1> sizes;
-    // keyed on the largest shared memory a call can ask for, so one answer
-    // serves every call
-    (void)smem;
-    return sizes.get([] {
+    return sizes.get([fn] {
         for (int cs : {kLcMaxCluster, 8}) {
-            if (cs > 8 && cudaFuncSetAttribute((const void *)layout_cluster_kernel,
-                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
                 cudaGetLastError();
                 continue;
             }
@@ -340,13 +342,18 @@ int cluster_size_for(size_t smem)
             cfg.attrs = &at;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, (const void *)layout_cluster_kernel, &cfg) == cudaSuccess &&
-                n > 0)
+            if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0)
                 return cs;
             cudaGetLastError();
         }
         return -1;  // cached: this device cannot run the kernel as a cluster
     });
+}
+
+int cluster_size_for()
+{
+    const int a = cluster_size_of<false>(), b = cluster_size_of<true>();
+    return a < b ? a : b;
 }
 
 }  // namespace
@@ -355,7 +362,7 @@ bool layout_cluster_supported(int T, int k, int E, int epr)
 {
     if (T < 1 || k < 1 || E < 1 || E > kLcMaxExperts || epr < 1 || E % epr != 0)
         return false;
-    const int cs = cluster_size_for(kLcMaxSmem);
+    const int cs = cluster_size_for();
     if (cs < 1)
         return false;
     const int B = (T + kBlk - 1) / kBlk;
@@ -369,7 +376,7 @@ cudaError_t launch_layout_cluster(const int32_t *topk_idx, int T, int k, int E, 
                                   int32_t *rank_off, int32_t *rank_tokens, int32_t *expert_dropped, int32_t *pos,
                                   int32_t *src, int32_t *err_flag, cudaStream_t st)
 {
-    const int cs = cluster_size_for(kLcMaxSmem);
+    const int cs = cluster_size_for();
     if (cs < 1)
         return cudaErrorNotSupported;
     const int B = (T + kBlk - 1) / kBlk;
@@ -408,7 +415,9 @@ cudaError_t launch_layout_cluster(const int32_t *topk_idx, int T, int k, int E, 
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, a);
+    if (cap >= 0)
+        return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<false>, a);
 }
 
 }  // namespace ep
